@@ -1,0 +1,178 @@
+/*
+ * nvfp4.h -- C ABI of the GB300 (sm_103a) NVFP4 W4A4 linear layer.
+ *
+ * What the library computes (the pages are vLLM pull-request summaries; each
+ * entry point names the one that defines its operation):
+ *
+ *   [torch-backend page]  "TorchNvFp4LinearKernel" (vLLM PR #53319), section
+ *       关键源码片段 (key source snippets): process_weights_after_loading
+ *       swizzles the weight block scales and pads the packed weight for the
+ *       GEMM; apply_weights quantizes the activation with its global scale into
+ *       packed FP4 plus swizzled block scales (K padded to the weight's padding),
+ *       runs the block-scaled FP4 GEMM into the activation dtype, multiplies by
+ *       alpha (product of the activation and weight global dequant scales),
+ *       slices the padded output columns and adds the bias.
+ *   [transform page]  "QUTLASS fusedQuantizeNv" (vLLM PR #43229), sections
+ *       实现拆解 (implementation breakdown) items 3, 4 and 6 and the
+ *       HadamardTransform snippet: an online block-diagonal transform of the
+ *       input (block size 16/32/64/128, 1/sqrt(n) folded into the matrix, result
+ *       in the activation dtype) fused with the NVFP4 quantization, writing into
+ *       caller-preallocated outputs that never alias the inputs.
+ *   [b12x page]  "B12X quantized linear backends" (vLLM PR #52016), NVFP4
+ *       snippet: a non-contiguous 2-D view of the input goes straight into the
+ *       quantizer (no contiguous copy); alpha is handed to the GEMM.
+ *
+ * Number formats.  FP4 = E2M1 (values 0, 0.5, 1, 1.5, 2, 3, 4, 6 and their
+ * negatives), two per byte, the even-index element in the low nibble.  Block
+ * scale = FP8 E4M3 (max 448) per 16 consecutive K elements.  The per-tensor
+ * global scale gs is an fp32 that MULTIPLIES into the block scale:
+ *     s  = (amax(block) * gs) / 6      (fp32, each op rounded to nearest even)
+ *     sf = e4m3_rne_satfinite(s)
+ *     q  = e2m1_rne_satfinite(v * (gs / e4m3(sf)))   (0 when e4m3(sf) == 0)
+ * so that v ~= e2m1(q) * e4m3(sf) / gs, and the linear's alpha = 1/(gs_x*gs_w).
+ *
+ * Layouts (all row-major, all caller-allocated device memory):
+ *   Kp  = roundup(k, 32)                 padded K of every packed operand
+ *   packed FP4   [rows, Kp/2] bytes      (row stride Kp/2; pad elements = 0)
+ *   scales       [Rp, Cp] bytes, tiled:  Rp = roundup(rows,128), Cp = roundup(Kp/16,4)
+ *       offset(r,c) = ((r/128)*(Cp/4) + c/4)*512 + (r%32)*16 + ((r%128)/32)*4 + c%4
+ *       i.e. 512-byte tiles of 128 rows x 4 scale columns; padding bytes are 0.
+ *
+ * Conventions shared by every call:
+ *   - Every pointer is device memory except where stated.  Buffers are owned
+ *     by the caller; the library allocates nothing and never synchronises the
+ *     stream: work is enqueued on `stream` (a cudaStream_t, 0 = legacy default).
+ *   - All arguments are validated on the host before anything is launched; an
+ *     invalid call returns a non-zero status, launches nothing and leaves the
+ *     reason in nvfp4_last_error_string() (thread-local).
+ *   - Outputs may not overlap any input (NVFP4_ERR_ALIAS).
+ *   - Row strides are in elements; every base pointer and every row must start
+ *     on a 16-byte boundary (NVFP4_ERR_ALIGNMENT).
+ *   - m == 0 (or n == 0 for the weight) is a valid empty call: NVFP4_OK, no launch.
+ *   - Global scales and alpha are read on the device (no host sync), which
+ *     keeps every call capturable in a CUDA graph.
+ *   - A kernel that waits longer than about a second on one of its own
+ *     pipeline barriers abandons the launch and raises a device error flag
+ *     that nvfp4_device_error() reports (NVFP4_ERR_TIMEOUT); it never hangs.
+ */
+#ifndef NVFP4_GB300_H
+#define NVFP4_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define NVFP4_ABI_VERSION 1
+
+/* Opaque CUDA stream handle; pass a cudaStream_t. */
+typedef struct CUstream_st *nvfp4_stream_t;
+
+typedef enum {
+    NVFP4_OK = 0,
+    NVFP4_ERR_INVALID_ARG = 1,        /* null pointer, bad size, bad block size  */
+    NVFP4_ERR_UNSUPPORTED_DEVICE = 2, /* current device is not compute 10.3       */
+    NVFP4_ERR_ALIGNMENT = 3,          /* pointer or row stride not 16-B aligned   */
+    NVFP4_ERR_ALIAS = 4,              /* an output overlaps an input              */
+    NVFP4_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed        */
+    NVFP4_ERR_TIMEOUT = 6,            /* a kernel gave up on a barrier wait       */
+    NVFP4_ERR_WORKSPACE = 7           /* workspace missing or too small           */
+} nvfp4_status;
+
+/* ABI version of the loaded library (NVFP4_ABI_VERSION at build time). */
+int nvfp4_abi_version(void);
+
+/* Capability check, modelled on the torch-backend page's is_supported (which
+ * returns (False, reason) instead of raising): NVFP4_OK if `device` can run
+ * this library (compute capability 10.3, the only target it is built for),
+ * else NVFP4_ERR_UNSUPPORTED_DEVICE / NVFP4_ERR_CUDA with a reason copied into
+ * `reason` (host buffer of reason_len bytes, may be NULL). */
+nvfp4_status nvfp4_is_supported(int device, char *reason, size_t reason_len);
+
+/* Text of the last error raised by a call on this host thread ("" if none).
+ * The string stays valid until the next library call on the same thread. */
+const char *nvfp4_last_error_string(void);
+
+/* Reads (and, if clear != 0, resets) the device error flag of the current
+ * device: NVFP4_OK or NVFP4_ERR_TIMEOUT.  This call synchronises the device. */
+nvfp4_status nvfp4_device_error(int clear);
+
+/* ---- size queries (pure host arithmetic; no device access) -------------- */
+
+/* Bytes of a packed FP4 operand: rows * roundup(k,32)/2. */
+size_t nvfp4_packed_bytes(int64_t rows, int64_t k);
+
+/* Bytes of a tiled scale tensor: roundup(rows,128) * roundup(roundup(k,32)/16, 4). */
+size_t nvfp4_scale_bytes(int64_t rows, int64_t k);
+
+/* Workspace nvfp4_linear needs for an m x k activation against n_w weight
+ * rows: the quantized activation and its scales (each 256-B aligned inside). */
+size_t nvfp4_linear_workspace_bytes(int64_t m, int64_t k, int64_t n_w);
+
+/* ---- operations ---------------------------------------------------------- */
+
+/* Weight preparation, the torch-backend page's process_weights_after_loading
+ * (swizzle_blockscale + pad_nvfp4_weight_for_cutlass), here starting from the
+ * bf16 weight: quantize W [n, k] (row stride ldw) with global scale *w_gs_dev
+ * (device fp32; the weight's counterpart of the activation global scale), pad
+ * K to Kp = roundup(k,32) with zeros, pack to FP4 and write the tiled scales.
+ *   w_bf16  in   [n, ldw] bf16
+ *   w_fp4   out  nvfp4_packed_bytes(n, k) bytes
+ *   w_sf    out  nvfp4_scale_bytes(n, k) bytes
+ * Outputs are written in place, so a reload into the same buffers keeps the
+ * weight addresses stable for captured graphs (b12x page, packed-storage reuse). */
+nvfp4_status nvfp4_prepare_weight(const void *w_bf16, int64_t n, int64_t k, int64_t ldw,
+                                  const float *w_gs_dev, uint8_t *w_fp4, uint8_t *w_sf,
+                                  nvfp4_stream_t stream);
+
+/* Activation quantization, the torch-backend page's scaled_fp4_quant call
+ * (swizzled scales, K padded) with the transform page's optional fused
+ * block-diagonal transform in front:
+ *   x_bf16          in   [m, ldx] bf16, the first k columns are the data (a
+ *                        strided view is fine: ldx >= k)
+ *   gs_dev          in   device fp32, activation global scale
+ *   transform_bf16  in   NULL (bs = 0) for none, else a bs x bs bf16 matrix T,
+ *                        row-major, 1/sqrt(bs) already folded in; bs in
+ *                        {16,32,64,128} and bs must divide k.  Then every bs-wide
+ *                        block of a row is replaced by y = bf16(x_block * T),
+ *                        accumulated in fp32 in index order, before quantizing.
+ *   x_fp4           out  nvfp4_packed_bytes(m, k) bytes
+ *   x_sf            out  nvfp4_scale_bytes(m, k) bytes                        */
+nvfp4_status nvfp4_quant_act(const void *x_bf16, int64_t m, int64_t k, int64_t ldx,
+                             const float *gs_dev, const void *transform_bf16, int bs,
+                             uint8_t *x_fp4, uint8_t *x_sf, nvfp4_stream_t stream);
+
+/* Block-scaled FP4 GEMM with the fused epilogue (torch-backend page:
+ * torch._scaled_mm, then * alpha, slice_nvfp4_output, + bias):
+ *   out[i, j] = bf16( alpha * sum_k deq(A)[i,k] * deq(W)[j,k] + bias[j] ),
+ *   deq(q) = e2m1(q) * e4m3(block scale), i < m, j < n_out.
+ *   a_fp4, a_sf     in   quantized activation (as written by nvfp4_quant_act)
+ *   w_fp4, w_sf     in   prepared weight with n_w rows (nvfp4_prepare_weight)
+ *   k               in   logical K of both (their Kp = roundup(k,32) must match)
+ *   n_out           in   1 <= n_out <= n_w: columns kept (the output slice)
+ *   alpha_dev       in   device fp32
+ *   bias_bf16       in   NULL or [n_out] bf16
+ *   out_bf16        out  [m, ldo] bf16, ldo >= n_out; columns >= n_out untouched */
+nvfp4_status nvfp4_gemm(const uint8_t *a_fp4, const uint8_t *a_sf, int64_t m,
+                        const uint8_t *w_fp4, const uint8_t *w_sf, int64_t n_w, int64_t n_out,
+                        int64_t k, const float *alpha_dev, const void *bias_bf16,
+                        void *out_bf16, int64_t ldo, nvfp4_stream_t stream);
+
+/* The whole linear layer (torch-backend page apply_weights; b12x page
+ * _apply_b12x_nvfp4_linear): nvfp4_quant_act of x into `workspace`, then
+ * nvfp4_gemm, both on `stream`.  workspace (device, >= nvfp4_linear_workspace_bytes)
+ * is scratch owned by the caller; its contents after the call are unspecified. */
+nvfp4_status nvfp4_linear(const void *x_bf16, int64_t m, int64_t k, int64_t ldx,
+                          const float *gs_dev, const void *transform_bf16, int bs,
+                          const uint8_t *w_fp4, const uint8_t *w_sf, int64_t n_w, int64_t n_out,
+                          const float *alpha_dev, const void *bias_bf16,
+                          void *out_bf16, int64_t ldo,
+                          void *workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_GB300_H */
