@@ -1,0 +1,515 @@
+"""Benchmark of the NVFP4 W4A4 linear on GB300 (one JSON line on rank 0).
+
+A step is one pass of the whole hot path over one batch: the four decoder
+linears of a Llama-3.1-8B-shaped layer (qkv 4096->6144, o 4096->4096,
+gate_up 4096->28672, down 14336->4096) at M = 8192 tokens, each through
+nvfp4_linear (activation quantization + block-scaled FP4 GEMM with the
+alpha/bias/bf16 epilogue).  Weights are prepared once, outside the timed region.
+
+  value      whole-job NVFP4-linear throughput, sum(2*M*N*K) / time, with the
+             inputs resident in HBM (per-rank inputs of 0.4 GB: larger than L2)
+  roofline   the GEMM kernel: its algorithmic FLOPs / its own CUDA-event time,
+             against the dense-FP4 peak (measured bf16 peak x the nominal
+             FP4:bf16 ratio 13.5/2.25 = 6)
+  act_quant  the activation quantizer: algorithmic bytes / its CUDA-event time,
+             against the measured HBM copy bandwidth
+  e2e        the same metric through nvfp4_linear with the activation copied in
+             from pinned host memory and the output copied back, every step
+  cpu_baseline  the CPU oracle (single thread) on a bounded sample of the same
+             workload: sampled rows x sampled output columns of each linear
+
+--impl reference times that oracle as the reference arm.  Under torchrun
+(N > 1) every rank runs its own batch (weak scaling, no data-path collective);
+only the barrier and the max-over-ranks time reduction touch the network.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "NVFP4 linear TFLOP/s (frac of FP4 peak); act-quant GB/s (frac of HBM peak)"
+WORKLOAD_M = 8192
+FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense FP4 : bf16 tensor rate of GB300
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+CPU_SAMPLE_ROWS = 16                 # cpu_baseline sample: rows x columns of every linear
+CPU_SAMPLE_COLS = 1024
+REF_STEP_ROWS = 2                    # reference arm: rows per linear per step
+REF_STEP_COLS = 512
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "gemm_llama_m8192_traffic.txt")
+
+
+# ------------------------------------------------------------ host logic ----
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--m", type=int, default=WORKLOAD_M, help="tokens per rank")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true")
+    a = ap.parse_args(argv)
+    a.warmup = max(a.warmup, 3)
+    return a
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def rank_seed(seed: int, rank: int) -> int:
+    """Each rank draws its own activations (data-parallel over tokens)."""
+    return seed + 7919 * rank
+
+
+def max_over_ranks(v: float, device) -> float:
+    """Slowest rank's time (all ranks call this; a no-op without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(per_rank_units: float, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: units of all ranks over the slowest rank's time."""
+    return per_rank_units * world / max_seconds
+
+
+def layer_problems(m: int, rank: int = 0):
+    from nvfp4_quantized_linear_gb300 import synthetic as syn
+    out = []
+    for p in syn.llama([m]):
+        out.append(syn.Problem(p.workload, p.name, p.m, p.k, p.n, seed=rank_seed(p.seed, rank)))
+    return out
+
+
+def quant_bytes(m: int, k: int) -> int:
+    """Algorithmic bytes of one activation quantization: bf16 read, packed FP4
+    and tiled scales written."""
+    kp = (k + 31) // 32 * 32
+    mp = (m + 127) // 128 * 128
+    nbp = (kp // 16 + 3) // 4 * 4
+    return 2 * m * k + m * kp // 2 + mp * nbp
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "MEASURED_PEAKS.json (measured)"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "profiling-recipe fallback"
+
+
+def gemm_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("gemm.cu", "ptx.cuh", "common.cuh"):
+        with open(os.path.join(ROOT, "nvfp4_quantized_linear_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per GEMM launch of the step's layers from the committed ncu
+    summary, if it was taken on the current GEMM source; else None."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            kv = dict(line.split(":", 1) for line in f if ":" in line and not line.startswith("#"))
+        if kv.get("gemm_source_hash", "").strip() != gemm_source_hash():
+            return None
+        return float(kv["dram_bytes_per_step_gemm"].strip())
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            self.proc.wait(timeout=10)
+        self.file.flush()
+
+    def summary(self):
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == 9:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        loaded = [s for s in sm if s > 0.5 * max(sm)] if sm else []
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": float(rows[0][2]) if rows[0][2].replace(".", "").isdigit() else None,
+                "power_w_max": max((float(r[3]) for r in rows if r[3].replace(".", "").isdigit()), default=None),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------- oracle ----
+
+class OracleSample:
+    """The CPU oracle on `rows` activation rows x `cols` output columns of each
+    linear (weights of the sampled columns quantized once, untimed)."""
+
+    def __init__(self, problems, rows: int, cols: int, seed: int = 0):
+        import numpy as np
+        import oracle
+        from nvfp4_quantized_linear_gb300 import synthetic as syn
+        oracle.build()
+        self.oracle, self.np = oracle, np
+        self.layers = []
+        rng = np.random.default_rng(seed)
+        for p in problems:
+            # the sampled activation rows and weight rows are drawn with the
+            # layer's own generators, so they are the same tensors the GPU sees
+            x = syn.make_activation(p, device="cpu", m=min(p.m, 4 * rows))
+            w = syn.bf16_normal((p.n, p.k), 0.02, p.seed + 100_000)
+            c = np.sort(rng.choice(p.n, size=min(cols, p.n), replace=False))
+            gs_x, gs_w = syn.global_scale(x), syn.global_scale(w)
+            b, sb = oracle.quantize(syn.bf16_bits(w[c]), gs_w)
+            self.layers.append(dict(p=p, x=syn.bf16_bits(x), b=b, sb=sb, gs_x=gs_x, alpha=syn.alpha_of(gs_x, gs_w),
+                                    ncols=len(c)))
+        self.rows = rows
+
+    def flops(self) -> int:
+        return sum(2 * self.rows * L["ncols"] * L["p"].k for L in self.layers)
+
+    def run(self, step: int = 0):
+        for L in self.layers:
+            n = L["x"].shape[0]
+            r = [(step * self.rows + i) % n for i in range(self.rows)]
+            a, sa = self.oracle.quantize(L["x"][r], L["gs_x"])
+            self.oracle.gemm(a, sa, L["b"], L["sb"], L["alpha"])
+
+
+def time_oracle(sample: OracleSample, min_seconds: float = 10.0, max_reps: int = 50):
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        sample.run(reps)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or reps >= max_reps:
+            return sample.flops() * reps / el / 1e12, el, reps
+
+
+# ------------------------------------------------------------------ GPU ----
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import nvfp4_quantized_linear_gb300 as nv
+    from nvfp4_quantized_linear_gb300 import synthetic as syn
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    nv.build()
+    ok, why = nv.nvfp4_is_supported(local_rank)
+    if not ok:
+        raise RuntimeError(why)
+    peaks, peak_src = load_peaks()
+    fp4_peak = peaks["bf16_tflops_sustained"] * FP4_OVER_BF16
+    fp4_peak_burst = peaks["bf16_tflops"] * FP4_OVER_BF16
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def slowest(v: float) -> float:
+        return max_over_ranks(v, dev)
+
+    problems = layer_problems(args.m, rank)
+    layers = []
+    for p in problems:
+        L = syn.make_layer(p, device=dev)
+        gs_x = torch.tensor([L.gs_x], dtype=torch.float32, device=dev)
+        gs_w = torch.tensor([L.gs_w], dtype=torch.float32, device=dev)
+        alpha = torch.tensor([L.alpha], dtype=torch.float32, device=dev)
+        w_fp4, w_sf = nv.prepare_weight(L.w, gs_w)
+        ws = torch.empty(nv.nvfp4_linear_workspace_bytes(p.m, p.k, p.n), dtype=torch.uint8, device=dev)
+        kp = nv.padded_k(p.k)
+        a_fp4 = ws[:p.m * kp // 2]
+        a_sf = ws[(p.m * kp // 2 + 255) // 256 * 256:]
+        out = torch.empty((p.m, p.n), dtype=torch.bfloat16, device=dev)
+        layers.append(dict(p=p, x=L.x, gs_x=gs_x, alpha=alpha, w_fp4=w_fp4, w_sf=w_sf, ws=ws, a_fp4=a_fp4,
+                           a_sf=a_sf, out=out))
+        del L
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream().cuda_stream
+    flops_step = sum(l["p"].flops for l in layers)
+
+    def linear(l):
+        p = l["p"]
+        nv.nvfp4_linear(l["x"], p.m, p.k, p.k, l["gs_x"], None, 0, l["w_fp4"], l["w_sf"], p.n, p.n, l["alpha"],
+                        None, l["out"], p.n, l["ws"], l["ws"].numel(), stream)
+
+    def split(l, ev):
+        p = l["p"]
+        ev[0].record()
+        nv.nvfp4_quant_act(l["x"], p.m, p.k, p.k, l["gs_x"], None, 0, l["a_fp4"], l["a_sf"], stream)
+        ev[1].record()
+        nv.nvfp4_gemm(l["a_fp4"], l["a_sf"], p.m, l["w_fp4"], l["w_sf"], p.n, p.n, p.k, l["alpha"], None,
+                      l["out"], p.n, stream)
+        ev[2].record()
+
+    for _ in range(args.warmup):
+        for l in layers:
+            linear(l)
+    torch.cuda.synchronize()
+    nv.nvfp4_device_error()
+
+    sampler = ClockSampler(local_rank)
+    with sampler:
+        # (A) the step through nvfp4_linear: value and ms_per_step
+        barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            for l in layers:
+                linear(l)
+        e1.record()
+        torch.cuda.synchronize()
+        barrier()
+        t_step = e0.elapsed_time(e1) / 1e3 / args.steps
+        # (B) the same kernels launched one by one, each bracketed by events on
+        # the launching stream: per-kernel durations for the roofline
+        evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in layers]
+               for _ in range(args.steps)]
+        barrier()
+        torch.cuda.synchronize()
+        for s in range(args.steps):
+            for i, l in enumerate(layers):
+                split(l, evs[s][i])
+        torch.cuda.synchronize()
+        barrier()
+    nv.nvfp4_device_error()
+    clocks = sampler.summary()
+
+    t_quant = [sum(evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(args.steps)) / args.steps / 1e3
+               for i in range(len(layers))]
+    t_gemm = [sum(evs[s][i][1].elapsed_time(evs[s][i][2]) for s in range(args.steps)) / args.steps / 1e3
+              for i in range(len(layers))]
+    t_step_max = slowest(t_step)
+    value = aggregate(flops_step, world, t_step_max) / 1e12
+    gemm_tflops = sum(l["p"].flops for l in layers) / sum(t_gemm) / 1e12
+    q_bytes = sum(quant_bytes(l["p"].m, l["p"].k) for l in layers)
+    quant_gbs = q_bytes / sum(t_quant) / 1e9
+    traffic_step = recorded_traffic()
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_step_max * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4",
+        "data": "synthetic",
+        "config": {"workload": f"llama3.1-8b decoder linears qkv/o/gate_up/down, M={args.m} tokens per GPU",
+                   "m": args.m, "layers": [[l["p"].name, l["p"].k, l["p"].n] for l in layers],
+                   "l2": "inputs larger than L2 (0.4 GB of activations per step)", "bias": False,
+                   "transform": None},
+        "roofline": {"bound": "tensor", "kernel": "gemm_nvf4_kernel",
+                     "achieved": round(gemm_tflops, 2), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
+                     "frac": round(gemm_tflops / fp4_peak, 4),
+                     "traffic": (round(traffic_step / len(layers)) if traffic_step else None),
+                     "peak_note": (f"dense FP4 = sustained bf16 {peaks['bf16_tflops_sustained']} x {FP4_OVER_BF16:g} "
+                                   f"from {peak_src}; burst-based {fp4_peak_burst:.0f}, nominal 13500"),
+                     "frac_of_nominal_13p5": round(gemm_tflops / 13500.0, 4)},
+        "act_quant": {"bound": "hbm", "kernel": "quant_kernel", "achieved": round(quant_gbs, 1),
+                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(quant_gbs / peaks["hbm_gbs"], 4),
+                      "bytes_per_step": q_bytes},
+        "per_layer": [{"layer": l["p"].name, "m": l["p"].m, "k": l["p"].k, "n": l["p"].n,
+                       "quant_us": round(tq * 1e6, 2), "gemm_us": round(tg * 1e6, 2),
+                       "gemm_tflops": round(l["p"].flops / tg / 1e12, 1),
+                       "quant_gbs": round(quant_bytes(l["p"].m, l["p"].k) / tq / 1e9, 1)}
+                      for l, tq, tg in zip(layers, t_quant, t_gemm)],
+        "gpu_launches": 2 * len(layers) * args.steps,
+        "clocks": clocks,
+    }
+
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, layers, flops_step, barrier, slowest, world, stream)
+    if not args.no_sweep:
+        result["m_sweep"] = run_sweep(args, rank, dev, stream)
+    del layers
+    torch.cuda.empty_cache()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample = OracleSample(layer_problems(args.m, 0), CPU_SAMPLE_ROWS, CPU_SAMPLE_COLS)
+        v, el, reps = time_oracle(sample)
+        result["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                                  "sample": f"{CPU_SAMPLE_ROWS} rows x {CPU_SAMPLE_COLS} output columns of each of "
+                                            f"the 4 linears (act quant + FP64 GEMM), {reps} reps in {el:.1f} s"}
+    return result
+
+
+def run_e2e(args, layers, flops_step, barrier, slowest, world, stream):
+    """Through the public API with host buffers: pinned H2D of every layer's
+    activation, nvfp4_linear, D2H of its output -- all inside the timed region."""
+    import torch
+
+    import nvfp4_quantized_linear_gb300 as nv
+    steps = max(3, min(args.steps, 10))
+    hx = [l["x"].cpu().pin_memory() for l in layers]
+    ho = [torch.empty(l["out"].shape, dtype=torch.bfloat16).pin_memory() for l in layers]
+    h2d = sum(h.numel() * 2 for h in hx)
+    d2h = sum(h.numel() * 2 for h in ho)
+
+    def step():
+        for l, x_h, o_h in zip(layers, hx, ho):
+            p = l["p"]
+            l["x"].copy_(x_h, non_blocking=True)
+            nv.nvfp4_linear(l["x"], p.m, p.k, p.k, l["gs_x"], None, 0, l["w_fp4"], l["w_sf"], p.n, p.n,
+                            l["alpha"], None, l["out"], p.n, l["ws"], l["ws"].numel(), stream)
+            o_h.copy_(l["out"], non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier()
+    t = slowest(e0.elapsed_time(e1) / 1e3 / steps)
+    return {"value": round(aggregate(flops_step, world, t) / 1e12, 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": round(t * 1e3, 3)}
+
+
+def run_sweep(args, rank, dev, stream):
+    """Decode/prefill-size breakdown: the same four linears at smaller M (not the
+    headline value)."""
+    import torch
+
+    import nvfp4_quantized_linear_gb300 as nv
+    from nvfp4_quantized_linear_gb300 import synthetic as syn
+    out = []
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for m in [1, 16, 128, 1024]:
+        layers = []
+        for p in layer_problems(m, rank):
+            L = syn.make_layer(p, device=dev)
+            gs_x = torch.tensor([L.gs_x], dtype=torch.float32, device=dev)
+            alpha = torch.tensor([L.alpha], dtype=torch.float32, device=dev)
+            w_fp4, w_sf = nv.prepare_weight(L.w, torch.tensor([L.gs_w], dtype=torch.float32, device=dev))
+            ws = torch.empty(nv.nvfp4_linear_workspace_bytes(p.m, p.k, p.n), dtype=torch.uint8, device=dev)
+            o = torch.empty((p.m, p.n), dtype=torch.bfloat16, device=dev)
+            layers.append((p, L.x, gs_x, alpha, w_fp4, w_sf, ws, o))
+
+        def step():
+            for p, x, gs_x, alpha, w_fp4, w_sf, ws, o in layers:
+                nv.nvfp4_linear(x, p.m, p.k, p.k, gs_x, None, 0, w_fp4, w_sf, p.n, p.n, alpha, None, o, p.n,
+                                ws, ws.numel(), stream)
+
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        # The four layers' weights (~116 MB of FP4 + scales) would stay in the
+        # 129 MB L2 across back-to-back steps; a real decoder streams them from
+        # HBM, so L2 is flushed before every timed step.
+        iters = 30
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+        for e0, e1 in evs:
+            flush.zero_()
+            e0.record()
+            step()
+            e1.record()
+        torch.cuda.synchronize()
+        t = sum(e0.elapsed_time(e1) for e0, e1 in evs) / 1e3 / iters
+        flops = sum(p.flops for p, *_ in layers)
+        wbytes = sum(w.numel() + s.numel() for _, _, _, _, w, s, _, _ in layers)
+        abytes = sum(quant_bytes(p.m, p.k) + 2 * p.m * p.n for p, *_ in layers)
+        out.append({"m": m, "us_per_step": round(t * 1e6, 2), "tflops": round(flops / t / 1e12, 2),
+                    "algorithmic_gbs": round((wbytes + abytes) / t / 1e9, 1), "l2": "flushed before each step"})
+        del layers
+    return out
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle, as it stands, on a bounded sample of
+    the same workload per step (rank 0 only)."""
+    if rank != 0:
+        return None
+    sample = OracleSample(layer_problems(args.m, 0), REF_STEP_ROWS, REF_STEP_COLS)
+    for s in range(args.warmup):
+        sample.run(s)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        sample.run(args.warmup + s)
+    el = time.perf_counter() - t0
+    value = sample.flops() * args.steps / el / 1e12
+    desc = (f"{REF_STEP_ROWS} rows x {REF_STEP_COLS} output columns of each of the 4 linears per step "
+            "(act quant + FP64 GEMM), single thread")
+    return {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": f"llama3.1-8b decoder linears qkv/o/gate_up/down, M={args.m} tokens per GPU",
+                       "m": args.m, "sample": desc},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local_rank = dist_env()
+    if world > 1 and args.impl == "ours":
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_ours(args, rank, world, local_rank)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

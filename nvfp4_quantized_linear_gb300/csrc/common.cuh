@@ -1,0 +1,66 @@
+// Internal declarations shared by the kernels and the C-ABI layer.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace nvfp4 {
+
+// Padded K of packed operands: a multiple of 32 FP4 elements (16 bytes), the
+// row alignment the TMA needs for the packed rows.
+__host__ __device__ constexpr int64_t padded_k(int64_t k) { return (k + 31) / 32 * 32; }
+// Scale columns (one per 16 elements of the padded K) and their padding to 4.
+__host__ __device__ constexpr int64_t scale_cols(int64_t k) { return padded_k(k) / 16; }
+__host__ __device__ constexpr int64_t scale_cols_padded(int64_t k) { return (scale_cols(k) + 3) / 4 * 4; }
+__host__ __device__ constexpr int64_t rows_padded(int64_t rows) { return (rows + 127) / 128 * 128; }
+
+// Byte offset of block scale (r, c) in the tiled scale layout: 512-byte tiles
+// of 128 rows x 4 columns, the tiles of a 128-row band consecutive along K;
+// inside a tile, 16-byte line (r % 32) holds rows r%32 + {0,32,64,96}, four
+// bytes each.  This is exactly the 32-row x 128-bit image that tcgen05.cp
+// (32x128b, warpx4) moves into TMEM for the block-scaled MMA.
+__host__ __device__ __forceinline__ int64_t sf_offset(int64_t r, int64_t c, int64_t cols_padded)
+{
+    return ((r >> 7) * (cols_padded >> 2) + (c >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (c & 3);
+}
+
+struct QuantParams {
+    const uint16_t *x;     // bf16 bits, [m, ldx]
+    int64_t ldx;           // elements
+    int32_t m, k;          // logical rows / K
+    int32_t kp;            // padded K
+    int32_t nb;            // kp / 16
+    int32_t nbp;           // roundup(nb, 4)
+    int32_t mp;            // roundup(m, 128)
+    const float *gs;       // device fp32
+    uint8_t *out;          // [m, kp/2]
+    uint8_t *sf;           // tiled [mp, nbp]
+    const uint16_t *t;     // transform (bf16 bits) or nullptr
+    int32_t bs;
+};
+
+struct GemmParams {
+    int32_t m, n_w, n_out, kp;
+    int32_t num_k64;                 // kp / 64 rounded up (= scale_cols_padded / 4)
+    int32_t num_m_blk, num_n_blk;
+    const uint8_t *sfa, *sfb;        // tiled scales
+    int64_t sfa_band_bytes;          // bytes per 128-row band of scales
+    int64_t sfb_band_bytes;
+    const float *alpha;
+    const uint16_t *bias;            // bf16 bits or nullptr
+    uint16_t *out;                   // bf16 bits
+    int64_t ldo;
+    unsigned int *err_flag;          // device error word
+};
+
+// Launchers (return a cudaError_t; no host synchronisation).
+cudaError_t launch_quant(const QuantParams &p, int num_sms, cudaStream_t s);
+cudaError_t launch_quant_transform(const QuantParams &p, int num_sms, cudaStream_t s);
+cudaError_t launch_gemm(const GemmParams &p, const uint8_t *a, const uint8_t *w, int num_sms, cudaStream_t s,
+                        const char **why);
+
+// Device error word (bit 1: a pipeline wait timed out).
+constexpr unsigned int kErrTimeout = 1u;
+cudaError_t device_error_word(unsigned int **ptr);
+
+}  // namespace nvfp4

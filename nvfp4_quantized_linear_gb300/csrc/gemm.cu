@@ -1,0 +1,336 @@
+// Block-scaled FP4 GEMM with fused epilogue on the sm_103a tensor cores.
+//
+// Page "TorchNvFp4LinearKernel" (vLLM PR #53319), section 关键源码片段:
+// apply_weights computes torch._scaled_mm(x_fp4, weight.t(), scale_a, scale_b,
+// out_dtype), then out * alpha, slice_nvfp4_output, + bias.  Here that is one
+// kernel:
+//     out[m, n] = bf16( alpha * sum_k A[m,k] B[n,k] + bias[n] ),  n < n_out,
+// A, B packed E2M1 (K-major) with one UE4M3 scale per 16 K-elements.
+//
+// Design (one CTA per SM, persistent over output tiles of 128 x 256):
+//   warp 0      TMA producer: A tile 128 x 256 FP4 (16 KB), B tile 256 x 256 FP4
+//               (32 KB), both 128-byte swizzled, plus the matching 512-byte
+//               scale tiles by bulk copy, into a 4-stage shared-memory ring;
+//   warp 1      MMA issuer: tcgen05.cp moves the stage's scale tiles into TMEM,
+//               then 4 x tcgen05.mma (M=128, N=256, K=64, kind::mxf4nvf4,
+//               scale_vec::4X) accumulate into a 128 x 256 fp32 TMEM tile;
+//               tcgen05.commit releases the smem stage / signals the epilogue;
+//   warp 2      allocates and frees the 512 TMEM columns;
+//   warps 4..7  epilogue: tcgen05.ld of their 32-lane quarter, fma with alpha
+//               and bias, bf16 round, masked stores (rows < m, cols < n_out).
+// TMEM columns: [0,256) accumulator; stage s scales at 256 + 48 s (A: 16
+// columns = 4 K-steps x 4; B: 32 columns = 4 K-steps x 2 row-halves x 4).
+// Every mbarrier wait is bounded (about 2 s); on expiry the kernel raises the
+// device error word, drains what it issued and exits.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace nvfp4 {
+
+__device__ unsigned int g_error_word;
+
+cudaError_t device_error_word(unsigned int **ptr)
+{
+    return cudaGetSymbolAddress(reinterpret_cast<void **>(ptr), g_error_word);
+}
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBKBytes = 128;                 // 256 FP4 elements of K per stage
+constexpr int kStages = 4;
+constexpr uint32_t kABytes = kBM * kBKBytes;  // 16 KB
+constexpr uint32_t kBBytes = kBN * kBKBytes;  // 32 KB
+constexpr uint32_t kSfaBytes = 4 * 512;       // 4 K-steps of one 128-row band
+constexpr uint32_t kSfbBytes = 2 * 4 * 512;   // two 128-row bands
+constexpr uint32_t kOffA = 0;
+constexpr uint32_t kOffB = kOffA + kStages * kABytes;
+constexpr uint32_t kOffSfa = kOffB + kStages * kBBytes;
+constexpr uint32_t kOffSfb = kOffSfa + kStages * kSfaBytes;
+constexpr uint32_t kOffBar = kOffSfb + kStages * kSfbBytes;
+constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;   // barriers + alignment slack
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemSf = 256;
+constexpr uint32_t kSfColsPerStage = 48;
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr int kThreads = 256;
+
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+struct Tile {
+    int mb, nb;
+};
+
+// Tiles are walked in groups of 8 row bands so that the CTAs resident at one
+// time share A bands and B bands in L2.
+__device__ __forceinline__ Tile tile_coord(int tile, int num_m, int num_n)
+{
+    constexpr int G = 8;
+    const int per_group = G * num_n;
+    const int group = tile / per_group;
+    const int first_m = group * G;
+    const int gm = min(G, num_m - first_m);
+    const int within = tile - group * per_group;
+    return {first_m + within % gm, within / gm};
+}
+
+__device__ __forceinline__ uint32_t bf16_bits_rn(float f)
+{
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const GemmParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    uint64_t *empty = full + kStages;
+    uint64_t *tmem_full = empty + kStages;
+    uint64_t *tmem_empty = tmem_full + 1;
+    uint64_t *mma_done = tmem_empty + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(tmem_full, 1);
+        mbar_init(tmem_empty, 4);
+        mbar_init(mma_done, 1);
+        fence_mbarrier_init();
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+    }
+    if (warp == 2) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    const int num_tiles = p.num_m_blk * p.num_n_blk;
+    const int num_ks = (p.num_k64 + 3) / 4;
+    const int n_bands_w = (p.n_w + 127) / 128;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------------ producer --
+        const uint64_t pol_a = l2_policy_evict_last();
+        const uint64_t pol_b = l2_policy_evict_last();
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued_mask = 0, issued_phase = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            const Tile t = tile_coord(tile, p.num_m_blk, p.num_n_blk);
+            const int n_rows = min(kBN, p.n_out - t.nb * kBN);
+            const int halves = n_rows > 128 ? 2 : 1;
+            for (int ks = 0; ks < num_ks; ++ks) {
+                if (!mbar_wait(&empty[stage], phase ^ 1, p.err_flag, kErrTimeout, kWaitNs)) { ok = false; break; }
+                const int kcount = min(4, p.num_k64 - ks * 4);
+                const uint32_t sf_bytes = (uint32_t)kcount * 512;
+                mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes + sf_bytes * (1 + halves));
+                tma_load_2d(smem + kOffA + stage * kABytes, &tmA, &full[stage], ks * kBKBytes, t.mb * kBM, pol_a);
+                tma_load_2d(smem + kOffB + stage * kBBytes, &tmB, &full[stage], ks * kBKBytes, t.nb * kBN, pol_b);
+                bulk_load(smem + kOffSfa + stage * kSfaBytes, p.sfa + t.mb * p.sfa_band_bytes + (int64_t)ks * 2048,
+                          sf_bytes, &full[stage], pol_a);
+                for (int h = 0; h < halves; ++h) {
+                    const int band = t.nb * 2 + h;
+                    if (band < n_bands_w)
+                        bulk_load(smem + kOffSfb + stage * kSfbBytes + h * 2048,
+                                  p.sfb + band * p.sfb_band_bytes + (int64_t)ks * 2048, sf_bytes, &full[stage], pol_b);
+                }
+                issued_mask |= 1u << stage;
+                issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                if (++stage == kStages) { stage = 0; phase ^= 1; }
+            }
+        }
+        // Every copy this thread issued has landed before the CTA may exit.
+        for (int s = 0; s < kStages; ++s)
+            if (issued_mask & (1u << s))
+                mbar_wait(&full[s], (issued_phase >> s) & 1u, p.err_flag, kErrTimeout, kWaitNs);
+    } else if (warp == 1 && lane == 0) {
+        // ----------------------------------------------------------- MMA --
+        int stage = 0;
+        uint32_t phase = 0, acc_phase = 0;
+        const uint32_t a_base = smem_u32(smem + kOffA);
+        const uint32_t b_base = smem_u32(smem + kOffB);
+        const uint32_t sfa_base = smem_u32(smem + kOffSfa);
+        const uint32_t sfb_base = smem_u32(smem + kOffSfb);
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            const Tile t = tile_coord(tile, p.num_m_blk, p.num_n_blk);
+            const int n_rows = min(kBN, p.n_out - t.nb * kBN);
+            const int halves = n_rows > 128 ? 2 : 1;
+            const uint32_t idesc = halves == 2 ? idesc_nvf4(128, 256) : idesc_nvf4(128, 128);
+            if (!mbar_wait(tmem_empty, acc_phase ^ 1, p.err_flag, kErrTimeout, kWaitNs)) break;
+            tc_fence_after_sync();
+            for (int ks = 0; ks < num_ks; ++ks) {
+                if (!mbar_wait(&full[stage], phase, p.err_flag, kErrTimeout, kWaitNs)) { ok = false; break; }
+                tc_fence_after_sync();
+                const int kcount = min(4, p.num_k64 - ks * 4);
+                const uint32_t sf_col = tmem + kTmemSf + stage * kSfColsPerStage;
+                for (int kk = 0; kk < kcount; ++kk) {
+                    tc_cp_32x128b_warpx4(sf_col + kk * 4, smem_desc_sf(sfa_base + stage * kSfaBytes + kk * 512));
+                    for (int h = 0; h < halves; ++h)
+                        tc_cp_32x128b_warpx4(sf_col + 16 + kk * 8 + h * 4,
+                                             smem_desc_sf(sfb_base + stage * kSfbBytes + h * 2048 + kk * 512));
+                }
+                const uint64_t adesc = smem_desc_sw128(a_base + stage * kABytes);
+                const uint64_t bdesc = smem_desc_sw128(b_base + stage * kBBytes);
+                for (int kk = 0; kk < kcount; ++kk) {
+                    // K-step kk starts 32 bytes further into the swizzled 128-byte rows
+                    tc_mma_nvf4(tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc,
+                                sf_col + kk * 4, sf_col + 16 + kk * 8, (ks | kk) != 0);
+                }
+                tc_commit(&empty[stage]);
+                if (++stage == kStages) { stage = 0; phase ^= 1; }
+            }
+            if (!ok) break;
+            tc_commit(tmem_full);
+            acc_phase ^= 1;
+        }
+        // No MMA may still be running when the TMEM is released.
+        tc_commit(mma_done);
+        mbar_wait(mma_done, 0, p.err_flag, kErrTimeout, kWaitNs);
+    } else if (warp >= 4) {
+        // ------------------------------------------------------ epilogue --
+        const int q = warp & 3;
+        const float alpha = __ldg(p.alpha);
+        uint32_t acc_phase = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            const Tile t = tile_coord(tile, p.num_m_blk, p.num_n_blk);
+            const int n_rows = min(kBN, p.n_out - t.nb * kBN);
+            if (!mbar_wait(tmem_full, acc_phase, p.err_flag, kErrTimeout, kWaitNs)) break;
+            tc_fence_after_sync();
+            const int64_t row = (int64_t)t.mb * kBM + q * 32 + lane;
+            uint16_t *orow = p.out + row * p.ldo;
+            for (int c = 0; c < n_rows; c += 32) {
+                uint32_t r[32];
+                tmem_ld_32cols(tmem + ((uint32_t)(q * 32) << 16) + c, r);
+                tmem_ld_wait();
+                const int col0 = t.nb * kBN + c;
+                const int ncol = min(32, p.n_out - col0);
+                float b[32];
+                if (p.bias != nullptr && ncol == 32) {
+                    const uint4 *bp = reinterpret_cast<const uint4 *>(p.bias + col0);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const uint4 w = __ldg(bp + v);
+                        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            b[v * 8 + 2 * e] = __uint_as_float(ws[e] << 16);
+                            b[v * 8 + 2 * e + 1] = __uint_as_float(ws[e] & 0xFFFF0000u);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        b[j] = (p.bias != nullptr && j < ncol) ? __uint_as_float((uint32_t)p.bias[col0 + j] << 16) : 0.0f;
+                }
+                if (row < p.m) {
+                    if (ncol == 32) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint4 o;
+                            uint32_t *ow = &o.x;
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int j = v * 8 + 2 * e;
+                                const uint32_t lo = bf16_bits_rn(__fmaf_rn(__uint_as_float(r[j]), alpha, b[j]));
+                                const uint32_t hi = bf16_bits_rn(__fmaf_rn(__uint_as_float(r[j + 1]), alpha, b[j + 1]));
+                                ow[e] = lo | (hi << 16);
+                            }
+                            *reinterpret_cast<uint4 *>(orow + col0 + v * 8) = o;
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < ncol)
+                                orow[col0 + j] = (uint16_t)bf16_bits_rn(__fmaf_rn(__uint_as_float(r[j]), alpha, b[j]));
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tmem_empty);
+            acc_phase ^= 1;
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == 2) tmem_dealloc(tmem, kTmemCols);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// 2-D map over a packed FP4 operand [rows, row_bytes] with 128-byte-wide boxes
+// of `box_rows` rows, 128-byte swizzle, zero fill outside the tensor.
+bool make_operand_map(CUtensorMap *map, const void *base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows)
+{
+    auto encode = tensor_map_encoder();
+    if (encode == nullptr) return false;
+    cuuint64_t dims[2] = {row_bytes, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {(cuuint32_t)kBKBytes, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmParams &p, const uint8_t *a, const uint8_t *w, int num_sms, cudaStream_t s,
+                        const char **why)
+{
+    static int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        cudaError_t e =
+            cudaFuncSetAttribute(gemm_nvf4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    CUtensorMap tmA, tmB;
+    const uint64_t row_bytes = (uint64_t)p.kp / 2;
+    if (!make_operand_map(&tmA, a, row_bytes, (uint64_t)p.m, kBM) ||
+        !make_operand_map(&tmB, w, row_bytes, (uint64_t)p.n_w, kBN)) {
+        *why = "cuTensorMapEncodeTiled failed for an FP4 operand";
+        return cudaErrorInvalidValue;
+    }
+    const int tiles = p.num_m_blk * p.num_n_blk;
+    const int grid = tiles < num_sms ? tiles : num_sms;
+    gemm_nvf4_kernel<<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, p);
+    return cudaGetLastError();
+}
+
+}  // namespace nvfp4

@@ -258,28 +258,33 @@ void oracle_gemm(const uint8_t *A, const uint8_t *sfA, const uint8_t *B, const u
                  const uint16_t *bias, double *out)
 {
     const int64_t nb = Kp / 16, kb = Kp / 2;
-    double *a_deq = (double *)malloc(sizeof(double) * (size_t)Kp);
-    assert(a_deq);
+    /* dequantized copies of the selected A rows and of one B row at a time */
+    double *a_deq = (double *)malloc(sizeof(double) * (size_t)(Kp * (n_rows > 0 ? n_rows : 1)));
+    double *b_deq = (double *)malloc(sizeof(double) * (size_t)Kp);
+    assert(a_deq && b_deq);
     for (int64_t i = 0; i < n_rows; ++i) {
         const int64_t m = row_idx[i];
         for (int64_t k = 0; k < Kp; ++k) {
             uint8_t byte = A[m * kb + k / 2];
             uint8_t q = (k & 1) ? (byte >> 4) : (byte & 0xF);
-            a_deq[k] = oracle_dec_e2m1(q) * oracle_dec_e4m3(sfA[m * nb + k / 16]);
+            a_deq[i * Kp + k] = oracle_dec_e2m1(q) * oracle_dec_e4m3(sfA[m * nb + k / 16]);
         }
-        for (int64_t j = 0; j < n_cols; ++j) {
-            const int64_t n = col_idx[j];
-            double acc = 0.0;
-            for (int64_t k = 0; k < Kp; ++k) {
-                uint8_t byte = B[n * kb + k / 2];
-                uint8_t q = (k & 1) ? (byte >> 4) : (byte & 0xF);
-                double b = oracle_dec_e2m1(q) * oracle_dec_e4m3(sfB[n * nb + k / 16]);
-                acc += a_deq[k] * b;
-            }
+    }
+    for (int64_t j = 0; j < n_cols; ++j) {
+        const int64_t n = col_idx[j];
+        for (int64_t k = 0; k < Kp; ++k) {
+            uint8_t byte = B[n * kb + k / 2];
+            uint8_t q = (k & 1) ? (byte >> 4) : (byte & 0xF);
+            b_deq[k] = oracle_dec_e2m1(q) * oracle_dec_e4m3(sfB[n * nb + k / 16]);
+        }
+        for (int64_t i = 0; i < n_rows; ++i) {
+            double acc = 0.0;                          /* k ascending */
+            for (int64_t k = 0; k < Kp; ++k) acc += a_deq[i * Kp + k] * b_deq[k];
             double o = (double)alpha * acc;
             if (bias) o += (double)oracle_bf16_to_f32(bias[n]);
             out[i * n_cols + j] = o;
         }
     }
     free(a_deq);
+    free(b_deq);
 }

@@ -1,0 +1,108 @@
+"""End-to-end parity of nvfp4_linear (quantize + GEMM + epilogue) against the
+oracle, on every layer workload at its full size and in the launch path the
+benchmark uses.  The GPU computes whole outputs; the oracle recomputes sampled
+rows x sampled columns (tile edges included) from the same bf16 inputs, since
+rows of the activation and rows of the weight quantize independently."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from _helpers import (assert_gemm_close, bf16_to_f64, dev_scalar, nv, require_library, sample_indices, syn,
+                      tile_edges)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    return require_library()
+
+
+def run_and_check(p: syn.Problem, n_rows=48, n_cols=384):
+    L = syn.make_layer(p, device="cuda")
+    m, k, n_out = p.m, p.k, p.n_keep
+    w_fp4, w_sf = nv.prepare_weight(L.w, dev_scalar(L.gs_w))
+    t = L.t.cuda() if L.t is not None else None
+    out = nv.linear(L.x, w_fp4, w_sf, k, n_out, dev_scalar(L.gs_x), dev_scalar(L.alpha), L.bias, t, p.bs)
+    torch.cuda.synchronize()
+    nv.nvfp4_device_error()
+    rows = np.arange(m) if m <= n_rows else sample_indices(m, n_rows, p.seed, must=tile_edges(m, 128))
+    cols = np.arange(n_out) if n_out <= n_cols else sample_indices(n_out, n_cols, p.seed + 1,
+                                                                   must=tile_edges(n_out, 128))
+    ri = torch.from_numpy(rows).cuda()
+    ci = torch.from_numpy(cols).cuda()
+    xb = syn.bf16_bits(L.x[ri])
+    if t is not None:
+        xb = oracle.transform(xb, syn.bf16_bits(L.t), p.bs)
+    a, sa = oracle.quantize(xb, L.gs_x, k=k)
+    b, sb = oracle.quantize(syn.bf16_bits(L.w[ci]), L.gs_w, k=k)
+    bias = syn.bf16_bits(L.bias[ci]) if L.bias is not None else None
+    ref = oracle.gemm(a, sa, b, sb, L.alpha, bias)
+    got = bf16_to_f64(out[ri][:, ci])
+    return assert_gemm_close(got, ref, f"{p.workload}/{p.name} m={m}")
+
+
+def _ids(ps):
+    return [f"{p.workload}-{p.name}-m{p.m}" + (f"-n{p.n_out}" if p.n_out else "") for p in ps]
+
+
+TINY = syn.tiny()
+LLAMA = syn.llama()
+QWEN = syn.qwen()
+XFORM = syn.transform_fused()
+PADDED = syn.padded() + [p for p in syn.padded(n_out=10944) if p.m in (1, 128, 1024)]
+
+
+@pytest.mark.parametrize("p", TINY, ids=_ids(TINY))
+def test_tiny(p):
+    run_and_check(p)
+
+
+@pytest.mark.parametrize("p", LLAMA, ids=_ids(LLAMA))
+def test_llama_shapes(p):
+    run_and_check(p)
+
+
+@pytest.mark.parametrize("p", QWEN, ids=_ids(QWEN))
+def test_qwen_shapes(p):
+    run_and_check(p)
+
+
+@pytest.mark.parametrize("p", XFORM, ids=_ids(XFORM))
+def test_transform_shapes(p):
+    run_and_check(p)
+
+
+@pytest.mark.parametrize("p", PADDED, ids=_ids(PADDED))
+def test_padded_shapes(p):
+    run_and_check(p)
+
+
+def test_linear_reuses_caller_buffers_across_calls():
+    """Same output/workspace buffers, two different activations: the second
+    call fully overwrites the first (no stale scratch state)."""
+    p = syn.Problem("t", "reuse", 200, 1024, 512, seed=77)
+    L = syn.make_layer(p, device="cuda")
+    w_fp4, w_sf = nv.prepare_weight(L.w, dev_scalar(L.gs_w))
+    out = torch.empty((200, 512), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(nv.nvfp4_linear_workspace_bytes(200, 1024, 512), dtype=torch.uint8, device="cuda")
+    x2 = syn.bf16_normal((200, 1024), 1.0, seed=78, device="cuda")
+    for x in (L.x, x2):
+        nv.linear(x, w_fp4, w_sf, 1024, 512, dev_scalar(L.gs_x), dev_scalar(L.alpha), out=out, workspace=ws)
+        torch.cuda.synchronize()
+        a, sa = oracle.quantize(syn.bf16_bits(x), L.gs_x)
+        b, sb = oracle.quantize(syn.bf16_bits(L.w), L.gs_w)
+        assert_gemm_close(bf16_to_f64(out), oracle.gemm(a, sa, b, sb, L.alpha), "reuse")
+
+
+def test_linear_rejects_small_workspace():
+    x = torch.zeros((4, 64), dtype=torch.bfloat16, device="cuda")
+    w_fp4 = torch.zeros((128, 32), dtype=torch.uint8, device="cuda")
+    w_sf = torch.zeros(nv.nvfp4_scale_bytes(128, 64), dtype=torch.uint8, device="cuda")
+    out = torch.empty((4, 128), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(nv.Nvfp4Error) as e:
+        nv.nvfp4_linear(x, 4, 64, 64, dev_scalar(1.0), None, 0, w_fp4, w_sf, 128, 128, dev_scalar(1.0), None,
+                        out, 128, ws, 16)
+    assert e.value.status == 7
