@@ -125,8 +125,9 @@ nvfp4_status check_quant_args(const void *x, int64_t m, int64_t k, int64_t ldx, 
     if (m < 0 || m > kMaxDim) return fail(NVFP4_ERR_INVALID_ARG, "rows of %s out of range: %lld", xname, (long long)m);
     if (k < 1 || k > kMaxDim) return fail(NVFP4_ERR_INVALID_ARG, "k out of range: %lld", (long long)k);
     if (ldx < k) return fail(NVFP4_ERR_INVALID_ARG, "row stride of %s (%lld) < k (%lld)", xname, (long long)ldx, (long long)k);
-    if ((int64_t)((m + 127) / 128) * 128 * nvfp4::scale_cols_padded(k) > (int64_t(1) << 40))
-        return fail(NVFP4_ERR_INVALID_ARG, "tensor too large");
+    if ((int64_t)((m + 127) / 128) * 128 * nvfp4::scale_cols_padded(k) > (int64_t(1) << 40) ||
+        nvfp4::rows_padded(m) * ((nvfp4::padded_k(k) + 511) / 512) >= (int64_t(1) << 31))
+        return fail(NVFP4_ERR_INVALID_ARG, "tensor too large (%lld x %lld)", (long long)m, (long long)k);
     if (m == 0) return NVFP4_OK;
     if (!x || !gs || !x_fp4 || !x_sf) return fail(NVFP4_ERR_INVALID_ARG, "null pointer argument");
     if (bs != 0 || t != nullptr) {

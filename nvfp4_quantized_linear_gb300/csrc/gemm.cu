@@ -11,13 +11,17 @@
 //   warp 0      TMA producer: A tile 128 x 256 FP4 (16 KB), B tile 256 x 256 FP4
 //               (32 KB), both 128-byte swizzled, plus the matching 512-byte
 //               scale tiles by bulk copy, into a 4-stage shared-memory ring;
-//   warp 1      MMA issuer: tcgen05.cp moves the stage's scale tiles into TMEM,
-//               then 4 x tcgen05.mma (M=128, N=256, K=64, kind::mxf4nvf4,
-//               scale_vec::4X) accumulate into a 128 x 256 fp32 TMEM tile;
-//               tcgen05.commit releases the smem stage / signals the epilogue;
+//   warp 3      scale copier: tcgen05.cp moves the stage's scale tiles into
+//               that stage's TMEM columns and commits to sf_ready[stage];
+//   warp 1      MMA issuer: 4 x tcgen05.mma (M=128, N=256, K=64,
+//               kind::mxf4nvf4, scale_vec::4X) per stage accumulate into a
+//               128 x 256 fp32 TMEM tile; tcgen05.commit releases the smem
+//               stage / signals the epilogue;
 //   warp 2      allocates and frees the 512 TMEM columns;
 //   warps 4..7  epilogue: tcgen05.ld of their 32-lane quarter, fma with alpha
-//               and bias, bf16 round, masked stores (rows < m, cols < n_out).
+//               and bias, bf16 round into registers, release of the TMEM tile,
+//               then masked stores (rows < m, cols < n_out) that overlap the
+//               next tile's MMAs.
 // TMEM columns: [0,256) accumulator; stage s scales at 256 + 48 s (A: 16
 // columns = 4 K-steps x 4; B: 32 columns = 4 K-steps x 2 row-halves x 4).
 // Every mbarrier wait is bounded (about 2 s); on expiry the kernel raises the
@@ -52,13 +56,16 @@ constexpr uint32_t kOffA = 0;
 constexpr uint32_t kOffB = kOffA + kStages * kABytes;
 constexpr uint32_t kOffSfa = kOffB + kStages * kBBytes;
 constexpr uint32_t kOffSfb = kOffSfa + kStages * kSfaBytes;
-constexpr uint32_t kOffBar = kOffSfb + kStages * kSfbBytes;
+constexpr uint32_t kOffBias = kOffSfb + kStages * kSfbBytes;   // per epilogue warp: one tile of bias
+constexpr uint32_t kOffBar = kOffBias + 4 * kBN * 2;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;   // barriers + alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemSf = 256;
 constexpr uint32_t kSfColsPerStage = 48;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kThreads = 256;
+constexpr int kEpiWarp0 = 4;                  // warps 4..7: epilogue, one per TMEM lane quarter
+constexpr int kEpiWarps = 4;
 
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
@@ -92,10 +99,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kOffBar);
     uint64_t *empty = full + kStages;
-    uint64_t *tmem_full = empty + kStages;
+    uint64_t *sf_ready = empty + kStages;
+    uint64_t *tmem_full = sf_ready + kStages;
     uint64_t *tmem_empty = tmem_full + 1;
     uint64_t *mma_done = tmem_empty + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+    uint64_t *cp_done = mma_done + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(cp_done + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -104,10 +113,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&sf_ready[s], 1);
         }
         mbar_init(tmem_full, 1);
-        mbar_init(tmem_empty, 4);
+        mbar_init(tmem_empty, kEpiWarps);
         mbar_init(mma_done, 1);
+        mbar_init(cp_done, 1);
         fence_mbarrier_init();
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
@@ -146,27 +157,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_2d(smem + kOffB + stage * kBBytes, &tmB, &full[stage], ks * kBKBytes, t.nb * kBN, pol_b);
                 bulk_load(smem + kOffSfa + stage * kSfaBytes, p.sfa + t.mb * p.sfa_band_bytes + (int64_t)ks * 2048,
                           sf_bytes, &full[stage], pol_a);
-                for (int h = 0; h < halves; ++h) {
-                    const int band = t.nb * 2 + h;
-                    if (band < n_bands_w)
-                        bulk_load(smem + kOffSfb + stage * kSfbBytes + h * 2048,
-                                  p.sfb + band * p.sfb_band_bytes + (int64_t)ks * 2048, sf_bytes, &full[stage], pol_b);
-                }
+                for (int h = 0; h < halves; ++h)    // halves == 2 implies band t.nb*2+1 < n_bands_w
+                    bulk_load(smem + kOffSfb + stage * kSfbBytes + h * 2048,
+                              p.sfb + (t.nb * 2 + h) * p.sfb_band_bytes + (int64_t)ks * 2048, sf_bytes, &full[stage],
+                              pol_b);
                 issued_mask |= 1u << stage;
                 issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                 if (++stage == kStages) { stage = 0; phase ^= 1; }
             }
         }
+        (void)n_bands_w;
         // Every copy this thread issued has landed before the CTA may exit.
         for (int s = 0; s < kStages; ++s)
             if (issued_mask & (1u << s))
                 mbar_wait(&full[s], (issued_phase >> s) & 1u, p.err_flag, kErrTimeout, kWaitNs);
-    } else if (warp == 1 && lane == 0) {
-        // ----------------------------------------------------------- MMA --
+    } else if (warp == 3 && lane == 0) {
+        // ---------------------------------------------------- scale copier --
+        // Moves each stage's scale tiles from shared memory into that stage's
+        // TMEM columns, then commits to sf_ready[stage].  Running these copies
+        // from their own thread lets them overlap the MMA thread's work.  A
+        // stage's TMEM columns are rewritten only after the producer refilled
+        // the stage, i.e. after the MMAs that read them completed.
         int stage = 0;
-        uint32_t phase = 0, acc_phase = 0;
-        const uint32_t a_base = smem_u32(smem + kOffA);
-        const uint32_t b_base = smem_u32(smem + kOffB);
+        uint32_t phase = 0;
         const uint32_t sfa_base = smem_u32(smem + kOffSfa);
         const uint32_t sfb_base = smem_u32(smem + kOffSfb);
         bool ok = true;
@@ -174,9 +187,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Tile t = tile_coord(tile, p.num_m_blk, p.num_n_blk);
             const int n_rows = min(kBN, p.n_out - t.nb * kBN);
             const int halves = n_rows > 128 ? 2 : 1;
-            const uint32_t idesc = halves == 2 ? idesc_nvf4(128, 256) : idesc_nvf4(128, 128);
-            if (!mbar_wait(tmem_empty, acc_phase ^ 1, p.err_flag, kErrTimeout, kWaitNs)) break;
-            tc_fence_after_sync();
             for (int ks = 0; ks < num_ks; ++ks) {
                 if (!mbar_wait(&full[stage], phase, p.err_flag, kErrTimeout, kWaitNs)) { ok = false; break; }
                 tc_fence_after_sync();
@@ -188,6 +198,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_cp_32x128b_warpx4(sf_col + 16 + kk * 8 + h * 4,
                                              smem_desc_sf(sfb_base + stage * kSfbBytes + h * 2048 + kk * 512));
                 }
+                tc_commit(&sf_ready[stage]);
+                if (++stage == kStages) { stage = 0; phase ^= 1; }
+            }
+        }
+        tc_commit(cp_done);
+        mbar_wait(cp_done, 0, p.err_flag, kErrTimeout, kWaitNs);
+    } else if (warp == 1 && lane == 0) {
+        // ----------------------------------------------------------- MMA --
+        int stage = 0;
+        uint32_t phase = 0, acc_phase = 0;
+        const uint32_t a_base = smem_u32(smem + kOffA);
+        const uint32_t b_base = smem_u32(smem + kOffB);
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            const Tile t = tile_coord(tile, p.num_m_blk, p.num_n_blk);
+            const int n_rows = min(kBN, p.n_out - t.nb * kBN);
+            const uint32_t idesc = n_rows > 128 ? idesc_nvf4(128, 256) : idesc_nvf4(128, 128);
+            if (!mbar_wait(tmem_empty, acc_phase ^ 1, p.err_flag, kErrTimeout, kWaitNs)) break;
+            tc_fence_after_sync();
+            for (int ks = 0; ks < num_ks; ++ks) {
+                if (!mbar_wait(&sf_ready[stage], phase, p.err_flag, kErrTimeout, kWaitNs) ||
+                    !mbar_wait(&full[stage], phase, p.err_flag, kErrTimeout, kWaitNs)) { ok = false; break; }
+                tc_fence_after_sync();
+                const int kcount = min(4, p.num_k64 - ks * 4);
+                const uint32_t sf_col = tmem + kTmemSf + stage * kSfColsPerStage;
                 const uint64_t adesc = smem_desc_sw128(a_base + stage * kABytes);
                 const uint64_t bdesc = smem_desc_sw128(b_base + stage * kBBytes);
                 for (int kk = 0; kk < kcount; ++kk) {
@@ -205,62 +240,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         // No MMA may still be running when the TMEM is released.
         tc_commit(mma_done);
         mbar_wait(mma_done, 0, p.err_flag, kErrTimeout, kWaitNs);
-    } else if (warp >= 4) {
+    } else if (warp >= kEpiWarp0) {
         // ------------------------------------------------------ epilogue --
+        // Drain the whole 128 x 256 accumulator into registers as packed bf16
+        // (alpha and bias applied), release the TMEM to the MMA thread, and only
+        // then write the tile out, so the stores overlap the next tile's MMAs.
         const int q = warp & 3;
+        uint16_t *s_bias = reinterpret_cast<uint16_t *>(smem + kOffBias) + (warp - kEpiWarp0) * kBN;
         const float alpha = __ldg(p.alpha);
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             const Tile t = tile_coord(tile, p.num_m_blk, p.num_n_blk);
             const int n_rows = min(kBN, p.n_out - t.nb * kBN);
+            const int col_base = t.nb * kBN;
+            if (p.bias != nullptr) {                            // this warp's copy of the tile's bias
+                __syncwarp();                                   // previous tile done reading it
+                for (int j = lane; j < kBN; j += 32)
+                    s_bias[j] = (j < n_rows) ? p.bias[col_base + j] : (uint16_t)0;
+                __syncwarp();
+            }
             if (!mbar_wait(tmem_full, acc_phase, p.err_flag, kErrTimeout, kWaitNs)) break;
             tc_fence_after_sync();
-            const int64_t row = (int64_t)t.mb * kBM + q * 32 + lane;
-            uint16_t *orow = p.out + row * p.ldo;
-            for (int c = 0; c < n_rows; c += 32) {
-                uint32_t r[32];
-                tmem_ld_32cols(tmem + ((uint32_t)(q * 32) << 16) + c, r);
-                tmem_ld_wait();
-                const int col0 = t.nb * kBN + c;
-                const int ncol = min(32, p.n_out - col0);
-                float b[32];
-                if (p.bias != nullptr && ncol == 32) {
-                    const uint4 *bp = reinterpret_cast<const uint4 *>(p.bias + col0);
+            uint32_t packed[kBN / 2];
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        const uint4 w = __ldg(bp + v);
-                        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+            for (int ch = 0; ch < kBN / 32; ++ch) {
+                if (ch * 32 < n_rows) {                         // uniform across the warp
+                    uint32_t r[32];
+                    tmem_ld_32cols(tmem + ((uint32_t)(q * 32) << 16) + ch * 32, r);
+                    tmem_ld_wait();
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            b[v * 8 + 2 * e] = __uint_as_float(ws[e] << 16);
-                            b[v * 8 + 2 * e + 1] = __uint_as_float(ws[e] & 0xFFFF0000u);
+                    for (int j = 0; j < 32; j += 2) {
+                        float b0 = 0.0f, b1 = 0.0f;
+                        if (p.bias != nullptr) {
+                            const uint32_t bw = *reinterpret_cast<const uint32_t *>(s_bias + ch * 32 + j);
+                            b0 = __uint_as_float(bw << 16);
+                            b1 = __uint_as_float(bw & 0xFFFF0000u);
                         }
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        b[j] = (p.bias != nullptr && j < ncol) ? __uint_as_float((uint32_t)p.bias[col0 + j] << 16) : 0.0f;
-                }
-                if (row < p.m) {
-                    if (ncol == 32) {
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            uint4 o;
-                            uint32_t *ow = &o.x;
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int j = v * 8 + 2 * e;
-                                const uint32_t lo = bf16_bits_rn(__fmaf_rn(__uint_as_float(r[j]), alpha, b[j]));
-                                const uint32_t hi = bf16_bits_rn(__fmaf_rn(__uint_as_float(r[j + 1]), alpha, b[j + 1]));
-                                ow[e] = lo | (hi << 16);
-                            }
-                            *reinterpret_cast<uint4 *>(orow + col0 + v * 8) = o;
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (j < ncol)
-                                orow[col0 + j] = (uint16_t)bf16_bits_rn(__fmaf_rn(__uint_as_float(r[j]), alpha, b[j]));
+                        const uint32_t lo = bf16_bits_rn(__fmaf_rn(__uint_as_float(r[j]), alpha, b0));
+                        const uint32_t hi = bf16_bits_rn(__fmaf_rn(__uint_as_float(r[j + 1]), alpha, b1));
+                        packed[ch * 16 + j / 2] = lo | (hi << 16);
                     }
                 }
             }
@@ -268,6 +286,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(tmem_empty);
             acc_phase ^= 1;
+
+            const int64_t row = (int64_t)t.mb * kBM + q * 32 + lane;
+            if (row < p.m) {
+                uint16_t *orow = p.out + row * p.ldo + col_base;
+#pragma unroll
+                for (int v = 0; v < kBN / 8; ++v) {
+                    if (v * 8 + 8 <= n_rows) {
+                        *reinterpret_cast<uint4 *>(orow + v * 8) =
+                            make_uint4(packed[v * 4], packed[v * 4 + 1], packed[v * 4 + 2], packed[v * 4 + 3]);
+                    } else if (v * 8 < n_rows) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            if (v * 8 + e < n_rows)
+                                orow[v * 8 + e] = (uint16_t)(packed[v * 4 + e / 2] >> ((e & 1) * 16));
+                    }
+                }
+            }
         }
     }
 

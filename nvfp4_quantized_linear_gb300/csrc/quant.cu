@@ -24,23 +24,6 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// Eight bf16 of one row starting at column k0, widened to fp32; columns at or
-// beyond k read as zero (no access past the row's k-th element).
-__device__ __forceinline__ void load8(const uint16_t *row, int k0, int k, bool row_ok, float (&v)[8])
-{
-    if (row_ok && k0 + 8 <= k) {
-        const uint4 w = ld_stream_v4(row + k0);
-        v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x);
-        v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
-        v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z);
-        v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
-    } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            v[i] = (row_ok && k0 + i < k) ? __uint_as_float((uint32_t)row[k0 + i] << 16) : 0.0f;
-    }
-}
-
 // Scale code and element multiplier of a block with absolute maximum `amax`.
 __device__ __forceinline__ uint32_t block_scale(float amax, float gs, float &inv)
 {
@@ -60,58 +43,95 @@ __device__ __forceinline__ uint32_t quant8(const float (&v)[8], float inv)
 }
 
 // ---------------------------------------------------------------------------
-// Plain quantizer.  A warp task is one 256-element segment of one row: lane l
-// owns elements [8l, 8l+8) (one 16-byte load), lanes 2j and 2j+1 share block j
-// (one shuffle for the block maximum), every lane stores 4 packed bytes (the
-// warp writes 128 contiguous bytes) and lanes 0, 8, 16, 24 each store the 4
-// scale bytes of 4 consecutive blocks as one word of a 512-byte scale tile.
-// Tasks run over the padded row count so the scale rows beyond m are zeroed
-// (those rows store no packed data).  U tasks per warp are loaded before any
-// is processed to keep enough bytes in flight.
+// Plain quantizer.  A warp task is one 512-element segment of one row: lane l
+// owns block l of the segment (elements [16l, 16l+16), two 16-byte loads), so
+// the block maximum and the scale arithmetic are done once per block, in one
+// lane.  Each lane stores its 8 packed bytes (the warp writes 256 contiguous
+// bytes) and lanes 0, 4, 8, ... store the 4 scale bytes of 4 consecutive blocks
+// as one word of a 512-byte scale tile.  Tasks run over the padded row count
+// so the scale rows beyond m are zeroed (those rows store no packed data).  A
+// warp loads the raw bytes of U consecutive tasks before processing any of
+// them, to keep enough bytes in flight.
+struct Raw16 {
+    uint4 a, b;
+};
+
+__device__ __forceinline__ Raw16 load16(const uint16_t *row, int k0, int k, bool row_ok)
+{
+    Raw16 r;
+    if (row_ok && k0 + 16 <= k) {
+        r.a = ld_stream_v4(row + k0);
+        r.b = ld_stream_v4(row + k0 + 8);
+    } else {
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t lo = (row_ok && k0 + 2 * i < k) ? row[k0 + 2 * i] : 0u;
+            const uint32_t hi = (row_ok && k0 + 2 * i + 1 < k) ? row[k0 + 2 * i + 1] : 0u;
+            w[i] = lo | (hi << 16);
+        }
+        r.a = make_uint4(w[0], w[1], w[2], w[3]);
+        r.b = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+    return r;
+}
+
+__device__ __forceinline__ void unpack8(const uint4 &w, float (&v)[8])
+{
+    v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x);
+    v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+    v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z);
+    v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
+}
+
 template <int U>
 __global__ void __launch_bounds__(256) quant_kernel(const QuantParams p)
 {
     const int lane = threadIdx.x & 31;
-    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int nwarps = (int)((gridDim.x * blockDim.x) >> 5);
     const float gs = __ldg(p.gs);
-    const int segs = (p.kp + 255) >> 8;
-    const int64_t tasks = (int64_t)p.mp * segs;
+    const int segs = (p.kp + 511) >> 9;
+    const int tasks = p.mp * segs;                    // < 2^31: checked on the host
     const int64_t out_ld = p.kp >> 1;
 
-    for (int64_t base = warp * U; base < tasks; base += nwarps * U) {
-        float v[U][8];
+    for (int base = warp * U; base < tasks; base += nwarps * U) {
+        // (row, segment) of the first task; the next ones follow along the row
+        int r0 = base / segs;
+        int s0 = base - r0 * segs;
+        Raw16 raw[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int64_t t = base + u;
-            const int64_t r = t / segs;
-            const int k0 = (int)(t - r * segs) * 256 + lane * 8;
-            const bool row_ok = (t < tasks) && (r < p.m);
-            load8(row_ok ? p.x + r * p.ldx : p.x, k0, p.k, row_ok, v[u]);
+            int r = r0, s = s0 + u;
+            while (s >= segs) { s -= segs; ++r; }
+            const bool row_ok = (base + u < tasks) && (r < p.m);
+            raw[u] = load16(row_ok ? p.x + (int64_t)r * p.ldx : p.x, s * 512 + lane * 16, p.k, row_ok);
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int64_t t = base + u;
-            if (t >= tasks) break;                        // uniform across the warp
-            const int64_t r = t / segs;
-            const int seg = (int)(t - r * segs);
-            const int k0 = seg * 256 + lane * 8;
-
+            if (base + u >= tasks) break;                 // uniform across the warp
+            int r = r0, s = s0 + u;
+            while (s >= segs) { s -= segs; ++r; }
+            const int k0 = s * 512 + lane * 16;
+            float v0[8], v1[8];
+            unpack8(raw[u].a, v0);
+            unpack8(raw[u].b, v1);
             float amax = 0.0f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[u][i]));
-            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(v0[i]), fabsf(v1[i])));
             float inv;
             const uint32_t sf = block_scale(amax, gs, inv);
-            const uint32_t packed = quant8(v[u], inv);
-            if (r < p.m && k0 < p.kp)
-                *reinterpret_cast<uint32_t *>(p.out + r * out_ld + (k0 >> 1)) = packed;
-
-            const uint32_t s1 = __shfl_down_sync(kFull, sf, 2);
-            const uint32_t s2 = __shfl_down_sync(kFull, sf, 4);
-            const uint32_t s3 = __shfl_down_sync(kFull, sf, 6);
-            const int c = seg * 16 + (lane >> 1);
-            if ((lane & 7) == 0 && c < p.nb)
+            if (r < p.m && k0 < p.kp) {
+                uint2 pk;
+                pk.x = quant8(v0, inv);
+                pk.y = quant8(v1, inv);
+                *reinterpret_cast<uint2 *>(p.out + (int64_t)r * out_ld + (k0 >> 1)) = pk;
+            }
+            const uint32_t s1 = __shfl_down_sync(kFull, sf, 1);
+            const uint32_t s2 = __shfl_down_sync(kFull, sf, 2);
+            const uint32_t s3 = __shfl_down_sync(kFull, sf, 3);
+            const int c = s * 32 + lane;
+            if ((lane & 3) == 0 && c < p.nb)
                 *reinterpret_cast<uint32_t *>(p.sf + sf_offset(r, c, p.nbp)) = sf | (s1 << 8) | (s2 << 16) | (s3 << 24);
         }
     }
@@ -223,7 +243,7 @@ __global__ void __launch_bounds__(256) quant_transform_kernel(const QuantParams 
 cudaError_t launch_quant(const QuantParams &p, int num_sms, cudaStream_t s)
 {
     constexpr int U = 4;
-    const int64_t segs = (p.kp + 255) / 256;
+    const int64_t segs = (p.kp + 511) / 512;
     const int64_t tasks = (int64_t)p.mp * segs;
     const int64_t warps_needed = (tasks + U - 1) / U;
     int64_t blocks = (warps_needed + 7) / 8;
