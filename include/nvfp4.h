@@ -49,8 +49,8 @@
  *   - Row strides are in elements; every base pointer and every row must start
  *     on a 16-byte boundary (NVFP4_ERR_ALIGNMENT).
  *   - m == 0 (or n == 0 for the weight) is a valid empty call: NVFP4_OK, no launch.
- *   - Global scales and alpha are read on the device (no host sync), which
- *     keeps every call capturable in a CUDA graph.
+ *   - Global scales and alpha are read on the device, so no call waits for the
+ *     host or synchronises with it.
  *   - A kernel that waits longer than about a second on one of its own
  *     pipeline barriers abandons the launch and raises a device error flag
  *     that nvfp4_device_error() reports (NVFP4_ERR_TIMEOUT); it never hangs.
@@ -170,6 +170,31 @@ nvfp4_status nvfp4_linear(const void *x_bf16, int64_t m, int64_t k, int64_t ldx,
                           const float *alpha_dev, const void *bias_bf16,
                           void *out_bf16, int64_t ldo,
                           void *workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/* nvfp4_linear without a caller-provided workspace.  The pages have no
+ * counterpart to this entry point: it exists for callers that cannot allocate
+ * device memory -- a plugin whose host framework owns every device allocation
+ * and gives it only its inputs and outputs, or latency-critical code that
+ * must never call cudaMalloc (which can synchronise the device).  It computes
+ * exactly what nvfp4_linear computes (same arguments minus the workspace),
+ * using a scratch array built into the library instead of a workspace:
+ *   - The scratch is 16 MiB of device memory that every GPU loading the
+ *     library holds until the process exits.  Calls whose workspace need
+ *     (nvfp4_linear_workspace_bytes(m, k, n_w)) exceeds it are rejected with
+ *     NVFP4_ERR_WORKSPACE before anything runs, e.g. up to m = 2048 at
+ *     k = 14336 or m = 8192 at k = 3584 fit.
+ *   - The first call on a device looks up the scratch's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - It allocates nothing (no cudaMalloc / cudaFree, no allocating library
+ *     call).  Every call on a device shares the one scratch array and leaves
+ *     its contents behind; calls whose work overlaps on the GPU (e.g. on two
+ *     streams) race on it. */
+nvfp4_status nvfp4_linear_noalloc(const void *x_bf16, int64_t m, int64_t k, int64_t ldx,
+                                  const float *gs_dev, const void *transform_bf16, int bs,
+                                  const uint8_t *w_fp4, const uint8_t *w_sf, int64_t n_w, int64_t n_out,
+                                  const float *alpha_dev, const void *bias_bf16,
+                                  void *out_bf16, int64_t ldo, nvfp4_stream_t stream);
 
 #ifdef __cplusplus
 }

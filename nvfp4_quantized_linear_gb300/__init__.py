@@ -22,7 +22,7 @@ __all__ = [
     "NVFP4_OK", "Nvfp4Error", "library_path", "load_library", "build",
     "nvfp4_abi_version", "nvfp4_is_supported", "nvfp4_last_error_string", "nvfp4_device_error",
     "nvfp4_packed_bytes", "nvfp4_scale_bytes", "nvfp4_linear_workspace_bytes",
-    "nvfp4_prepare_weight", "nvfp4_quant_act", "nvfp4_gemm", "nvfp4_linear",
+    "nvfp4_prepare_weight", "nvfp4_quant_act", "nvfp4_gemm", "nvfp4_linear", "nvfp4_linear_noalloc",
     "padded_k", "scale_shape",
 ]
 
@@ -51,6 +51,8 @@ EXPORTS = [
     ("nvfp4_gemm", _I32, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _P, _P, _I64, _P]),
     ("nvfp4_linear", _I32, [_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _I64, _I64, _P, _P, _P, _I64,
                             _P, _SZ, _P]),
+    ("nvfp4_linear_noalloc", _I32, [_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _I64, _I64, _P, _P, _P, _I64,
+                                    _P]),
 ]
 
 
@@ -181,6 +183,16 @@ def nvfp4_linear(x, m: int, k: int, ldx: int, gs, transform, bs: int, w_fp4, w_s
     _check(load_library().nvfp4_linear(_ptr(x), m, k, ldx, _ptr(gs), _ptr(transform), bs, _ptr(w_fp4),
                                        _ptr(w_sf), n_w, n_out, _ptr(alpha), _ptr(bias), _ptr(out), ldo,
                                        _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def nvfp4_linear_noalloc(x, m: int, k: int, ldx: int, gs, transform, bs: int, w_fp4, w_sf, n_w: int, n_out: int,
+                         alpha, bias, out, ldo: int, stream=None) -> None:
+    """nvfp4_linear with the library's built-in 16 MiB scratch instead of a
+    workspace, for callers that cannot allocate device memory (see the C
+    header for the limit and the sharing rules)."""
+    _check(load_library().nvfp4_linear_noalloc(_ptr(x), m, k, ldx, _ptr(gs), _ptr(transform), bs, _ptr(w_fp4),
+                                               _ptr(w_sf), n_w, n_out, _ptr(alpha), _ptr(bias), _ptr(out), ldo,
+                                               _stream(stream)))
 
 
 # --------------------------------------------- tensor-level conveniences ----

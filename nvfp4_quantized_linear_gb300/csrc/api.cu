@@ -245,6 +245,12 @@ size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
 }  // namespace
 
+int nvfp4::record_error(int st, const char *msg)
+{
+    g_last_error = msg;
+    return st;
+}
+
 extern "C" {
 
 int nvfp4_abi_version(void) { return NVFP4_ABI_VERSION; }

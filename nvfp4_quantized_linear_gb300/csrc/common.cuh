@@ -59,6 +59,10 @@ cudaError_t launch_quant_transform(const QuantParams &p, int num_sms, cudaStream
 cudaError_t launch_gemm(const GemmParams &p, const uint8_t *a, const uint8_t *w, int num_sms, cudaStream_t s,
                         const char **why);
 
+// Records `msg` as this thread's last error (read by nvfp4_last_error_string)
+// and returns `st`; for entry points that live outside api.cu.
+int record_error(int st, const char *msg);
+
 // Device error word (bit 1: a pipeline wait timed out).
 constexpr unsigned int kErrTimeout = 1u;
 cudaError_t device_error_word(unsigned int **ptr);
