@@ -4,6 +4,7 @@
 #include <algorithm>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -14,6 +15,14 @@
 namespace {
 
 thread_local std::string g_last_error;
+
+// GEMMs run on the one-CTA kernel.  NVFP4_GEMM_PAIR=1 in the environment (read
+// once, when the library loads) sends GEMMs with m > 128 to the CTA-pair kernel
+// instead, which computes the same result.
+const bool g_use_pair_kernel = [] {
+    const char *v = getenv("NVFP4_GEMM_PAIR");
+    return v != nullptr && v[0] == '1';
+}();
 
 nvfp4_status fail(nvfp4_status st, const char *fmt, ...)
 {
@@ -236,7 +245,8 @@ nvfp4_status run_gemm(const uint8_t *a, const uint8_t *a_sf, int64_t m, const ui
     if (e != cudaSuccess) return launch_status(e, "GEMM (error word)");
     nvfp4::GemmParams g = gemm_params(a_sf, m, w_sf, n_w, n_out, k, alpha, bias, out, ldo, err);
     const char *why = nullptr;
-    e = nvfp4::launch_gemm(g, a, w, num_sms, s, &why);
+    e = (m > 128 && g_use_pair_kernel) ? nvfp4::launch_gemm_pair(g, a, w, num_sms, s, &why)
+                                       : nvfp4::launch_gemm(g, a, w, num_sms, s, &why);
     if (why) return fail(NVFP4_ERR_CUDA, "%s", why);
     return launch_status(e, "GEMM kernel");
 }

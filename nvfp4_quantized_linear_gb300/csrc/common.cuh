@@ -58,6 +58,9 @@ cudaError_t launch_quant(const QuantParams &p, int num_sms, cudaStream_t s);
 cudaError_t launch_quant_transform(const QuantParams &p, int num_sms, cudaStream_t s);
 cudaError_t launch_gemm(const GemmParams &p, const uint8_t *a, const uint8_t *w, int num_sms, cudaStream_t s,
                         const char **why);
+// CTA-pair variant for m > 128 (tiles of 256 x 256 on two SMs).
+cudaError_t launch_gemm_pair(const GemmParams &p, const uint8_t *a, const uint8_t *w, int num_sms, cudaStream_t s,
+                             const char **why);
 
 // Records `msg` as this thread's last error (read by nvfp4_last_error_string)
 // and returns `st`; for entry points that live outside api.cu.

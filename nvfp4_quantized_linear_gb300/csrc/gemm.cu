@@ -11,13 +11,14 @@
 //   warp 0      TMA producer: A tile 128 x 256 FP4 (16 KB), B tile 256 x 256 FP4
 //               (32 KB), both 128-byte swizzled, plus the matching 512-byte
 //               scale tiles by bulk copy, into a 4-stage shared-memory ring;
-//   warp 3      scale copier: tcgen05.cp moves the stage's scale tiles into
-//               that stage's TMEM columns and commits to sf_ready[stage];
+//   warps 2,3   scale copiers (lane 0 of each): tcgen05.cp moves the stage's
+//               scale tiles into that stage's TMEM columns, two K-steps per
+//               copier, and each commits to sf_ready[stage];
 //   warp 1      MMA issuer: 4 x tcgen05.mma (M=128, N=256, K=64,
 //               kind::mxf4nvf4, scale_vec::4X) per stage accumulate into a
 //               128 x 256 fp32 TMEM tile; tcgen05.commit releases the smem
 //               stage / signals the epilogue;
-//   warp 2      allocates and frees the 512 TMEM columns;
+//   warp 2      also allocates and frees the 512 TMEM columns;
 //   warps 4..7  epilogue: tcgen05.ld of their 32-lane quarter, fma with alpha
 //               and bias, bf16 round into registers, release of the TMEM tile,
 //               then masked stores (rows < m, cols < n_out) that overlap the
@@ -31,6 +32,7 @@
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
+#include "gemm_common.cuh"
 #include "ptx.cuh"
 
 namespace nvfp4 {
@@ -43,6 +45,8 @@ cudaError_t device_error_word(unsigned int **ptr)
 }
 
 namespace {
+
+using namespace gemm_detail;
 
 constexpr int kBM = 128;
 constexpr int kBN = 256;
@@ -66,30 +70,16 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kThreads = 256;
 constexpr int kEpiWarp0 = 4;                  // warps 4..7: epilogue, one per TMEM lane quarter
 constexpr int kEpiWarps = 4;
+constexpr int kCopiers = 2;                   // lane 0 of warps 2 and 3: two K-steps of each stage each
+
+// Copier index of a thread (-1 if it does not copy scales).  The copiers sit
+// in different warps: a warp issues a tcgen05 instruction for one lane only.
+__device__ __forceinline__ int copier_of(int warp, int lane)
+{
+    return lane == 0 ? (warp == 2 ? 0 : warp == 3 ? 1 : -1) : -1;
+}
 
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-
-struct Tile {
-    int mb, nb;
-};
-
-// Tiles are walked in groups of 8 row bands so that the CTAs resident at one
-// time share A bands and B bands in L2.
-__device__ __forceinline__ Tile tile_coord(int tile, int num_m, int num_n)
-{
-    constexpr int G = 8;
-    const int per_group = G * num_n;
-    const int group = tile / per_group;
-    const int first_m = group * G;
-    const int gm = min(G, num_m - first_m);
-    const int within = tile - group * per_group;
-    return {first_m + within % gm, within / gm};
-}
-
-__device__ __forceinline__ uint32_t bf16_bits_rn(float f)
-{
-    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
-}
 
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -113,12 +103,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
-            mbar_init(&sf_ready[s], 1);
+            mbar_init(&sf_ready[s], kCopiers);
         }
         mbar_init(tmem_full, 1);
         mbar_init(tmem_empty, kEpiWarps);
         mbar_init(mma_done, 1);
-        mbar_init(cp_done, 1);
+        mbar_init(cp_done, kCopiers);
         fence_mbarrier_init();
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
@@ -171,13 +161,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kStages; ++s)
             if (issued_mask & (1u << s))
                 mbar_wait(&full[s], (issued_phase >> s) & 1u, p.err_flag, kErrTimeout, kWaitNs);
-    } else if (warp == 3 && lane == 0) {
-        // ---------------------------------------------------- scale copier --
-        // Moves each stage's scale tiles from shared memory into that stage's
-        // TMEM columns, then commits to sf_ready[stage].  Running these copies
-        // from their own thread lets them overlap the MMA thread's work.  A
-        // stage's TMEM columns are rewritten only after the producer refilled
-        // the stage, i.e. after the MMAs that read them completed.
+    } else if (copier_of(warp, lane) >= 0) {
+        // --------------------------------------------------- scale copiers --
+        // Copier c moves K-steps 2c and 2c+1 of each stage (the A band's tile
+        // and the B bands' tiles) from shared memory into that stage's TMEM
+        // columns and commits to sf_ready[stage], which completes once both
+        // have.  Two issuing threads keep the copies off the MMA's critical path.
+        // A stage's TMEM columns are rewritten only after the producer
+        // refilled the stage, i.e. after the MMAs that read them completed.
+        const int cidx = copier_of(warp, lane);
         int stage = 0;
         uint32_t phase = 0;
         const uint32_t sfa_base = smem_u32(smem + kOffSfa);
@@ -192,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after_sync();
                 const int kcount = min(4, p.num_k64 - ks * 4);
                 const uint32_t sf_col = tmem + kTmemSf + stage * kSfColsPerStage;
-                for (int kk = 0; kk < kcount; ++kk) {
+                for (int kk = 2 * cidx; kk < 2 * cidx + 2 && kk < kcount; ++kk) {
                     tc_cp_32x128b_warpx4(sf_col + kk * 4, smem_desc_sf(sfa_base + stage * kSfaBytes + kk * 512));
                     for (int h = 0; h < halves; ++h)
                         tc_cp_32x128b_warpx4(sf_col + 16 + kk * 8 + h * 4,
@@ -310,35 +302,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
     if (warp == 2) tmem_dealloc(tmem, kTmemCols);
-}
-
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (fn == nullptr) {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
-    return fn;
-}
-
-// 2-D map over a packed FP4 operand [rows, row_bytes] with 128-byte-wide boxes
-// of `box_rows` rows, 128-byte swizzle, zero fill outside the tensor.
-bool make_operand_map(CUtensorMap *map, const void *base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows)
-{
-    auto encode = tensor_map_encoder();
-    if (encode == nullptr) return false;
-    cuuint64_t dims[2] = {row_bytes, rows};
-    cuuint64_t strides[1] = {row_bytes};
-    cuuint32_t box[2] = {(cuuint32_t)kBKBytes, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace

@@ -1,0 +1,69 @@
+// Pieces shared by the two GEMM kernels (one CTA per tile, and CTA pairs).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+
+namespace nvfp4 {
+namespace gemm_detail {
+
+struct Tile {
+    int mb, nb;
+};
+
+// Tiles are walked column by column (row band fastest) inside groups of up to
+// 64 row bands: the CTAs resident at one time work on a few weight column
+// bands, so each weight tile is streamed from DRAM about once and shared by
+// the row bands through L2, while the group's activation rows (at most 64
+// bands) stay resident in L2 across columns.
+__device__ __forceinline__ Tile tile_coord(int tile, int num_m, int num_n)
+{
+    const int G = num_m < 64 ? num_m : 64;
+    const int per_group = G * num_n;
+    const int group = tile / per_group;
+    const int first_m = group * G;
+    const int gm = min(G, num_m - first_m);
+    const int within = tile - group * per_group;
+    return {first_m + within % gm, within / gm};
+}
+
+__device__ __forceinline__ uint32_t bf16_bits_rn(float f)
+{
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+
+inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// 2-D map over a packed FP4 operand [rows, row_bytes] with 128-byte-wide boxes
+// of `box_rows` rows, 128-byte swizzle, zero fill outside the tensor.
+inline bool make_operand_map(CUtensorMap *map, const void *base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows)
+{
+    auto encode = tensor_map_encoder();
+    if (encode == nullptr) return false;
+    cuuint64_t dims[2] = {row_bytes, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {128u, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+
+}  // namespace gemm_detail
+}  // namespace nvfp4
