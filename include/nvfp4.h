@@ -107,8 +107,11 @@ size_t nvfp4_packed_bytes(int64_t rows, int64_t k);
 /* Bytes of a tiled scale tensor: roundup(rows,128) * roundup(roundup(k,32)/16, 4). */
 size_t nvfp4_scale_bytes(int64_t rows, int64_t k);
 
-/* Workspace nvfp4_linear needs for an m x k activation against n_w weight
- * rows: the quantized activation and its scales (each 256-B aligned inside). */
+/* Workspace nvfp4_linear wants for an m x k activation against n_w weight
+ * rows: the quantized activation and its scales (each 256-B aligned inside)
+ * and, for m <= 128, room for split-K partial sums (160 * 256 fp32 per row).
+ * nvfp4_linear accepts any workspace that holds the first two; given less than
+ * this size, a small-m call runs without split-K. */
 size_t nvfp4_linear_workspace_bytes(int64_t m, int64_t k, int64_t n_w);
 
 /* ---- operations ---------------------------------------------------------- */
@@ -162,8 +165,15 @@ nvfp4_status nvfp4_gemm(const uint8_t *a_fp4, const uint8_t *a_sf, int64_t m,
 
 /* The whole linear layer (torch-backend page apply_weights; b12x page
  * _apply_b12x_nvfp4_linear): nvfp4_quant_act of x into `workspace`, then
- * nvfp4_gemm, both on `stream`.  workspace (device, >= nvfp4_linear_workspace_bytes)
- * is scratch owned by the caller; its contents after the call are unspecified. */
+ * the GEMM of nvfp4_gemm, all on `stream`.  workspace (device) is scratch owned
+ * by the caller, at least align256(nvfp4_packed_bytes(m,k)) +
+ * align256(nvfp4_scale_bytes(m,k)) bytes (else NVFP4_ERR_WORKSPACE); its
+ * contents after the call are unspecified.  With m <= 128 and a workspace of
+ * nvfp4_linear_workspace_bytes, a GEMM whose output has too few 128 x 256
+ * tiles to fill the GPU splits K across CTAs: each writes fp32 partial sums to
+ * the workspace and a second kernel adds them in split order, then applies
+ * alpha and bias.  The result is deterministic, but its fp32 rounding order
+ * differs from the unsplit GEMM's (both are within the GEMM's accuracy). */
 nvfp4_status nvfp4_linear(const void *x_bf16, int64_t m, int64_t k, int64_t ldx,
                           const float *gs_dev, const void *transform_bf16, int bs,
                           const uint8_t *w_fp4, const uint8_t *w_sf, int64_t n_w, int64_t n_out,
@@ -179,8 +189,8 @@ nvfp4_status nvfp4_linear(const void *x_bf16, int64_t m, int64_t k, int64_t ldx,
  * exactly what nvfp4_linear computes (same arguments minus the workspace),
  * using a scratch array built into the library instead of a workspace:
  *   - The scratch is 16 MiB of device memory that every GPU loading the
- *     library holds until the process exits.  Calls whose workspace need
- *     (nvfp4_linear_workspace_bytes(m, k, n_w)) exceeds it are rejected with
+ *     library holds until the process exits.  Calls whose quantized activation
+ *     and scales (nvfp4_linear's minimum workspace) exceed it are rejected with
  *     NVFP4_ERR_WORKSPACE before anything runs, e.g. up to m = 2048 at
  *     k = 14336 or m = 8192 at k = 3584 fit.
  *   - The first call on a device looks up the scratch's device address

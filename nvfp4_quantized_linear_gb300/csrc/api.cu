@@ -233,27 +233,84 @@ nvfp4::GemmParams gemm_params(const uint8_t *a_sf, int64_t m, const uint8_t *w_s
     g.out = static_cast<uint16_t *>(out);
     g.ldo = ldo;
     g.err_flag = err;
+    g.splits = 1;
+    g.stages_per_split = (g.num_k64 + 3) / 4;
+    g.partials = nullptr;
+    g.part_ld = 0;
     return g;
 }
 
+// Split-K plan for small m (a single 128-row band): when the output has too
+// few 128 x 256 tiles to occupy every SM, cut K into ranges so that tiles x
+// splits is close to the SM count.  Returns the number of splits (1: none) and
+// sets the stages per split such that no range is empty.
+int split_k_plan(const nvfp4::GemmParams &g, int num_sms, int *stages_per_split)
+{
+    const int num_ks = (g.num_k64 + 3) / 4;
+    *stages_per_split = num_ks;
+    if (g.m > 128) return 1;
+    const int tiles = g.num_n_blk;
+    if (tiles * 2 > num_sms) return 1;
+    int s = num_sms / tiles;
+    if (s > num_ks) s = num_ks;
+    if (s > nvfp4::kMaxSplits) s = nvfp4::kMaxSplits;
+    if (s < 2) return 1;
+    const int sps = (num_ks + s - 1) / s;
+    *stages_per_split = sps;
+    return (num_ks + sps - 1) / sps;
+}
+
+// Bytes of split-K partial sums for a split plan.
+size_t split_k_bytes(const nvfp4::GemmParams &g, int splits)
+{
+    return (size_t)splits * (size_t)g.m * (size_t)g.num_n_blk * 256 * sizeof(float);
+}
+
+// Upper bound of split_k_bytes for any device of up to 160 SMs: splits x tiles
+// never exceeds the SM count, so the partials never exceed 160 x 256 floats per row.
+constexpr size_t kSplitBytesPerRow = 160 * 256 * sizeof(float);
+
+// Launches the GEMM; with `partials` (scratch of partial_bytes bytes) and a
+// small m it may split K and finish with the reduce kernel.  after_quant: the
+// kernel just before on `s` is the quantizer of `a` (and nothing else), so the
+// GEMM may start as its programmatic dependent.
 nvfp4_status run_gemm(const uint8_t *a, const uint8_t *a_sf, int64_t m, const uint8_t *w, const uint8_t *w_sf,
                       int64_t n_w, int64_t n_out, int64_t k, const float *alpha, const void *bias, void *out,
-                      int64_t ldo, int num_sms, cudaStream_t s)
+                      int64_t ldo, int num_sms, cudaStream_t s, float *partials = nullptr, size_t partial_bytes = 0,
+                      bool after_quant = false)
 {
     unsigned int *err = nullptr;
     cudaError_t e = nvfp4::device_error_word(&err);
     if (e != cudaSuccess) return launch_status(e, "GEMM (error word)");
     nvfp4::GemmParams g = gemm_params(a_sf, m, w_sf, n_w, n_out, k, alpha, bias, out, ldo, err);
+    if (partials != nullptr) {
+        int sps = 0;
+        const int splits = split_k_plan(g, num_sms, &sps);
+        if (splits > 1 && split_k_bytes(g, splits) <= partial_bytes) {
+            g.splits = splits;
+            g.stages_per_split = sps;
+            g.partials = partials;
+            g.part_ld = (int64_t)g.num_n_blk * 256;
+        }
+    }
     const char *why = nullptr;
     e = (m > 128 && g_use_pair_kernel) ? nvfp4::launch_gemm_pair(g, a, w, num_sms, s, &why)
-                                       : nvfp4::launch_gemm(g, a, w, num_sms, s, &why);
+                                       : nvfp4::launch_gemm(g, a, w, num_sms, s, &why, after_quant);
     if (why) return fail(NVFP4_ERR_CUDA, "%s", why);
-    return launch_status(e, "GEMM kernel");
+    nvfp4_status st = launch_status(e, "GEMM kernel");
+    if (st != NVFP4_OK || g.splits == 1) return st;
+    return launch_status(nvfp4::launch_splitk_reduce(g, num_sms, s), "split-K reduce kernel");
 }
 
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
 }  // namespace
+
+size_t nvfp4::linear_min_workspace_bytes(int64_t m, int64_t k)
+{
+    if (m <= 0 || k <= 0) return 0;
+    return align256(nvfp4_packed_bytes(m, k)) + align256(nvfp4_scale_bytes(m, k));
+}
 
 int nvfp4::record_error(int st, const char *msg)
 {
@@ -322,7 +379,8 @@ size_t nvfp4_linear_workspace_bytes(int64_t m, int64_t k, int64_t n_w)
 {
     (void)n_w;
     if (m <= 0 || k <= 0) return 0;
-    return align256(nvfp4_packed_bytes(m, k)) + align256(nvfp4_scale_bytes(m, k));
+    const size_t base = nvfp4::linear_min_workspace_bytes(m, k);
+    return m <= 128 ? base + align256(kSplitBytesPerRow * (size_t)m) : base;
 }
 
 nvfp4_status nvfp4_quant_act(const void *x_bf16, int64_t m, int64_t k, int64_t ldx, const float *gs_dev,
@@ -382,7 +440,7 @@ nvfp4_status nvfp4_linear(const void *x_bf16, int64_t m, int64_t k, int64_t ldx,
                           void *workspace, size_t workspace_bytes, nvfp4_stream_t stream)
 {
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    const size_t need = nvfp4_linear_workspace_bytes(m, k, n_w);
+    const size_t need = nvfp4::linear_min_workspace_bytes(m, k);   // quantized activation + scales
     uint8_t *a_fp4 = ws;
     uint8_t *a_sf = ws ? ws + align256(nvfp4_packed_bytes(m, k)) : nullptr;
     nvfp4_status st = check_quant_args(x_bf16, m, k, ldx, gs_dev, transform_bf16, bs, m > 0 ? a_fp4 : nullptr,
@@ -395,7 +453,7 @@ nvfp4_status nvfp4_linear(const void *x_bf16, int64_t m, int64_t k, int64_t ldx,
     if (m == 0) return ok();
     if (workspace_bytes < need)
         return fail(NVFP4_ERR_WORKSPACE, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, need);
-    Range outs[2] = {range2d(out_bf16, m, n_out, ldo, "out"), range(workspace, need, "workspace")};
+    Range outs[2] = {range2d(out_bf16, m, n_out, ldo, "out"), range(workspace, workspace_bytes, "workspace")};
     Range ins[7] = {range2d(x_bf16, m, k, ldx, "x"), range(gs_dev, 4, "gs"),
                     range(transform_bf16, transform_bf16 ? (size_t)bs * bs * 2 : 0, "transform"),
                     range(w_fp4, nvfp4_packed_bytes(n_w, k), "w_fp4"), range(w_sf, nvfp4_scale_bytes(n_w, k), "w_sf"),
@@ -406,7 +464,10 @@ nvfp4_status nvfp4_linear(const void *x_bf16, int64_t m, int64_t k, int64_t ldx,
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     st = run_quant(quant_params(x_bf16, m, k, ldx, gs_dev, transform_bf16, bs, a_fp4, a_sf), num_sms, s);
     if (st != NVFP4_OK) return st;
-    return run_gemm(a_fp4, a_sf, m, w_fp4, w_sf, n_w, n_out, k, alpha_dev, bias_bf16, out_bf16, ldo, num_sms, s);
+    // the rest of the workspace (if any) takes split-K partial sums
+    float *partials = workspace_bytes > need ? reinterpret_cast<float *>(ws + need) : nullptr;
+    return run_gemm(a_fp4, a_sf, m, w_fp4, w_sf, n_w, n_out, k, alpha_dev, bias_bf16, out_bf16, ldo, num_sms, s,
+                    partials, workspace_bytes > need ? workspace_bytes - need : 0, true);
 }
 
 }  // extern "C"

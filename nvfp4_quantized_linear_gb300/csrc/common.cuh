@@ -39,6 +39,8 @@ struct QuantParams {
     int32_t bs;
 };
 
+constexpr int kMaxSplits = 16;       // split-K ranges at most
+
 struct GemmParams {
     int32_t m, n_w, n_out, kp;
     int32_t num_k64;                 // kp / 64 rounded up (= scale_cols_padded / 4)
@@ -51,16 +53,34 @@ struct GemmParams {
     uint16_t *out;                   // bf16 bits
     int64_t ldo;
     unsigned int *err_flag;          // device error word
+    // Split-K (small m): K is cut into `splits` ranges of `stages_per_split`
+    // 256-element stages; each range writes raw fp32 sums (no alpha, bias or
+    // rounding) to partials[split][row][col] (row stride part_ld) and a reduce
+    // kernel finishes the epilogue.  splits == 1: the GEMM writes `out` itself.
+    int32_t splits;                  // 1 .. kMaxSplits
+    int32_t stages_per_split;
+    float *partials;
+    int64_t part_ld;
 };
 
 // Launchers (return a cudaError_t; no host synchronisation).
 cudaError_t launch_quant(const QuantParams &p, int num_sms, cudaStream_t s);
 cudaError_t launch_quant_transform(const QuantParams &p, int num_sms, cudaStream_t s);
+// dependent = true launches the GEMM as a programmatic dependent of the
+// preceding kernel, which must be the quantizer of its activation operand:
+// the GEMM's weight-side loads then start before that kernel has finished.
 cudaError_t launch_gemm(const GemmParams &p, const uint8_t *a, const uint8_t *w, int num_sms, cudaStream_t s,
-                        const char **why);
+                        const char **why, bool dependent = false);
+// Sum of the split-K partials, then alpha, bias and bf16 rounding into out;
+// launched as a programmatic dependent of the split GEMM just before it.
+cudaError_t launch_splitk_reduce(const GemmParams &p, int num_sms, cudaStream_t s);
 // CTA-pair variant for m > 128 (tiles of 256 x 256 on two SMs).
 cudaError_t launch_gemm_pair(const GemmParams &p, const uint8_t *a, const uint8_t *w, int num_sms, cudaStream_t s,
                              const char **why);
+
+// Smallest workspace nvfp4_linear accepts: the quantized activation and its
+// scales (256-byte aligned inside); anything beyond it holds split-K partials.
+size_t linear_min_workspace_bytes(int64_t m, int64_t k);
 
 // Records `msg` as this thread's last error (read by nvfp4_last_error_string)
 // and returns `st`; for entry points that live outside api.cu.

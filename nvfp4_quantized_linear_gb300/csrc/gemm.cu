@@ -7,22 +7,25 @@
 //     out[m, n] = bf16( alpha * sum_k A[m,k] B[n,k] + bias[n] ),  n < n_out,
 // A, B packed E2M1 (K-major) with one UE4M3 scale per 16 K-elements.
 //
-// Design (one CTA per SM, persistent over output tiles of 128 x 256):
+// Design (one CTA per SM, persistent over output tiles of 128 x 256; 12 warps):
 //   warp 0      TMA producer: A tile 128 x 256 FP4 (16 KB), B tile 256 x 256 FP4
 //               (32 KB), both 128-byte swizzled, plus the matching 512-byte
-//               scale tiles by bulk copy, into a 4-stage shared-memory ring;
-//   warps 2,3   scale copiers (lane 0 of each): tcgen05.cp moves the stage's
-//               scale tiles into that stage's TMEM columns, two K-steps per
-//               copier, and each commits to sf_ready[stage];
-//   warp 1      MMA issuer: 4 x tcgen05.mma (M=128, N=256, K=64,
-//               kind::mxf4nvf4, scale_vec::4X) per stage accumulate into a
-//               128 x 256 fp32 TMEM tile; tcgen05.commit releases the smem
-//               stage / signals the epilogue;
-//   warp 2      also allocates and frees the 512 TMEM columns;
-//   warps 4..7  epilogue: tcgen05.ld of their 32-lane quarter, fma with alpha
-//               and bias, bf16 round into registers, release of the TMEM tile,
-//               then masked stores (rows < m, cols < n_out) that overlap the
-//               next tile's MMAs.
+//               scale tiles by bulk copy, into a 4-stage shared-memory ring.
+//               The weight side of the first fills goes out before the wait
+//               on the preceding grid (programmatic dependent launch);
+//   warp 1      allocates / frees the 512 TMEM columns; lane 0 issues the
+//               MMAs: 4 x tcgen05.mma (M=128, N=256, K=64, kind::mxf4nvf4,
+//               scale_vec::4X) per stage into a 128 x 256 fp32 TMEM tile;
+//               tcgen05.commit releases the smem stage / signals the epilogue;
+//   warps 4..7  one per TMEM lane quarter: stage each landed stage's scale
+//               tiles into TMEM with tcgen05.st, keeping the tensor pipe for
+//               the MMAs alone;
+//   warps 8..11 epilogue, one per TMEM lane quarter: tcgen05.ld of finished
+//               accumulators, fma with alpha and bias, bf16 round into
+//               registers, release of the TMEM tile, then masked stores
+//               (rows < m, cols < n_out) that overlap the next tile's MMAs.
+//               With split-K the drain writes raw fp32 partial sums instead.
+// Registers are moved between the warpgroups at start (setmaxnreg).
 // TMEM columns: [0,256) accumulator; stage s scales at 256 + 48 s (A: 16
 // columns = 4 K-steps x 4; B: 32 columns = 4 K-steps x 2 row-halves x 4).
 // Every mbarrier wait is bounded (about 2 s); on expiry the kernel raises the
@@ -60,30 +63,47 @@ constexpr uint32_t kOffA = 0;
 constexpr uint32_t kOffB = kOffA + kStages * kABytes;
 constexpr uint32_t kOffSfa = kOffB + kStages * kBBytes;
 constexpr uint32_t kOffSfb = kOffSfa + kStages * kSfaBytes;
-constexpr uint32_t kOffBias = kOffSfb + kStages * kSfbBytes;   // per epilogue warp: one tile of bias
-constexpr uint32_t kOffBar = kOffBias + 4 * kBN * 2;
+constexpr uint32_t kOffBias = kOffSfb + kStages * kSfbBytes;   // two tiles of bias (bf16), double-buffered
+constexpr uint32_t kOutChunkBytes = 32 * 16 * 2;              // output staging: 32 rows x 16 columns bf16
+constexpr uint32_t kOffOut = kOffBias + 2 * kBN * 2;          // per epilogue warp: two staging chunks
+constexpr uint32_t kOffBar = kOffOut + 4 * 2 * kOutChunkBytes;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;   // barriers + alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemSf = 256;
 constexpr uint32_t kSfColsPerStage = 48;
 constexpr uint64_t kWaitNs = 2000000000ull;
-constexpr int kThreads = 256;
-constexpr int kEpiWarp0 = 4;                  // warps 4..7: epilogue, one per TMEM lane quarter
+constexpr int kThreads = 384;                 // three warpgroups
+constexpr int kSfWarp0 = 4;                   // warps 4..7: scale staging, lane quarter warp % 4
+constexpr int kEpiWarp0 = 8;                  // warps 8..11: epilogue, lane quarter warp % 4
 constexpr int kEpiWarps = 4;
-constexpr int kCopiers = 2;                   // lane 0 of warps 2 and 3: two K-steps of each stage each
-
-// Copier index of a thread (-1 if it does not copy scales).  The copiers sit
-// in different warps: a warp issues a tcgen05 instruction for one lane only.
-__device__ __forceinline__ int copier_of(int warp, int lane)
-{
-    return lane == 0 ? (warp == 2 ? 0 : warp == 3 ? 1 : -1) : -1;
-}
+// Registers per thread after the reallocation at kernel start (launched with
+// 65536 / 384 = 168): 128 x (56 + 96 + 240) = 50176 <= 384 x 168 = 64512.
+constexpr uint32_t kRegsCtl = 56, kRegsSf = 96, kRegsEpi = 240;
+static_assert(128 * (kRegsCtl + kRegsSf + kRegsEpi) <= kThreads * 168, "register reallocation budget");
 
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kOffOut % 128 == 0, "TMA store sources are 128-byte aligned");
+
+// Work item of a persistent CTA: output tile and K-stage range [ks0, ks1).
+struct Work {
+    Tile t;
+    int split, ks0, ks1;
+};
+
+__device__ __forceinline__ Work work_of(int item, const GemmParams &p, int num_ks)
+{
+    const int per_split = p.num_m_blk * p.num_n_blk;
+    Work w;
+    w.split = item / per_split;
+    w.t = tile_coord(item - w.split * per_split, p.num_m_blk, p.num_n_blk);
+    w.ks0 = w.split * p.stages_per_split;
+    w.ks1 = min(num_ks, w.ks0 + p.stages_per_split);
+    return w;
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const GemmParams p)
+                     const __grid_constant__ CUtensorMap tmOut, const GemmParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -93,8 +113,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *tmem_full = sf_ready + kStages;
     uint64_t *tmem_empty = tmem_full + 1;
     uint64_t *mma_done = tmem_empty + 1;
-    uint64_t *cp_done = mma_done + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(cp_done + 1);
+    uint64_t *bias_full = mma_done + 1;     // [2]
+    uint64_t *bias_empty = bias_full + 2;   // [2]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bias_empty + 2);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -103,17 +124,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
-            mbar_init(&sf_ready[s], kCopiers);
+            mbar_init(&sf_ready[s], 4);
         }
         mbar_init(tmem_full, 1);
         mbar_init(tmem_empty, kEpiWarps);
         mbar_init(mma_done, 1);
-        mbar_init(cp_done, kCopiers);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bias_full[b], 1);
+            mbar_init(&bias_empty[b], kEpiWarps);
+        }
         fence_mbarrier_init();
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
     }
-    if (warp == 2) {
+    if (warp == 1) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
@@ -122,192 +146,349 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    const int num_tiles = p.num_m_blk * p.num_n_blk;
+    const int num_tiles = p.num_m_blk * p.num_n_blk * p.splits;     // work items
     const int num_ks = (p.num_k64 + 3) / 4;
     const int n_bands_w = (p.n_w + 127) / 128;
 
-    if (warp == 0 && lane == 0) {
-        // ------------------------------------------------------ producer --
-        const uint64_t pol_a = l2_policy_evict_last();
-        const uint64_t pol_b = l2_policy_evict_last();
-        int stage = 0;
-        uint32_t phase = 0;
-        uint32_t issued_mask = 0, issued_phase = 0;
-        bool ok = true;
-        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-            const Tile t = tile_coord(tile, p.num_m_blk, p.num_n_blk);
-            const int n_rows = min(kBN, p.n_out - t.nb * kBN);
-            const int halves = n_rows > 128 ? 2 : 1;
-            for (int ks = 0; ks < num_ks; ++ks) {
-                if (!mbar_wait(&empty[stage], phase ^ 1, p.err_flag, kErrTimeout, kWaitNs)) { ok = false; break; }
-                const int kcount = min(4, p.num_k64 - ks * 4);
-                const uint32_t sf_bytes = (uint32_t)kcount * 512;
-                mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes + sf_bytes * (1 + halves));
-                tma_load_2d(smem + kOffA + stage * kABytes, &tmA, &full[stage], ks * kBKBytes, t.mb * kBM, pol_a);
-                tma_load_2d(smem + kOffB + stage * kBBytes, &tmB, &full[stage], ks * kBKBytes, t.nb * kBN, pol_b);
-                bulk_load(smem + kOffSfa + stage * kSfaBytes, p.sfa + t.mb * p.sfa_band_bytes + (int64_t)ks * 2048,
-                          sf_bytes, &full[stage], pol_a);
-                for (int h = 0; h < halves; ++h)    // halves == 2 implies band t.nb*2+1 < n_bands_w
-                    bulk_load(smem + kOffSfb + stage * kSfbBytes + h * 2048,
-                              p.sfb + (t.nb * 2 + h) * p.sfb_band_bytes + (int64_t)ks * 2048, sf_bytes, &full[stage],
-                              pol_b);
-                issued_mask |= 1u << stage;
-                issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-                if (++stage == kStages) { stage = 0; phase ^= 1; }
-            }
-        }
-        (void)n_bands_w;
-        // Every copy this thread issued has landed before the CTA may exit.
-        for (int s = 0; s < kStages; ++s)
-            if (issued_mask & (1u << s))
-                mbar_wait(&full[s], (issued_phase >> s) & 1u, p.err_flag, kErrTimeout, kWaitNs);
-    } else if (copier_of(warp, lane) >= 0) {
-        // --------------------------------------------------- scale copiers --
-        // Copier c moves K-steps 2c and 2c+1 of each stage (the A band's tile
-        // and the B bands' tiles) from shared memory into that stage's TMEM
-        // columns and commits to sf_ready[stage], which completes once both
-        // have.  Two issuing threads keep the copies off the MMA's critical path.
-        // A stage's TMEM columns are rewritten only after the producer
-        // refilled the stage, i.e. after the MMAs that read them completed.
-        const int cidx = copier_of(warp, lane);
-        int stage = 0;
-        uint32_t phase = 0;
-        const uint32_t sfa_base = smem_u32(smem + kOffSfa);
-        const uint32_t sfb_base = smem_u32(smem + kOffSfb);
-        bool ok = true;
-        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-            const Tile t = tile_coord(tile, p.num_m_blk, p.num_n_blk);
-            const int n_rows = min(kBN, p.n_out - t.nb * kBN);
-            const int halves = n_rows > 128 ? 2 : 1;
-            for (int ks = 0; ks < num_ks; ++ks) {
-                if (!mbar_wait(&full[stage], phase, p.err_flag, kErrTimeout, kWaitNs)) { ok = false; break; }
-                tc_fence_after_sync();
-                const int kcount = min(4, p.num_k64 - ks * 4);
-                const uint32_t sf_col = tmem + kTmemSf + stage * kSfColsPerStage;
-                for (int kk = 2 * cidx; kk < 2 * cidx + 2 && kk < kcount; ++kk) {
-                    tc_cp_32x128b_warpx4(sf_col + kk * 4, smem_desc_sf(sfa_base + stage * kSfaBytes + kk * 512));
-                    for (int h = 0; h < halves; ++h)
-                        tc_cp_32x128b_warpx4(sf_col + 16 + kk * 8 + h * 4,
-                                             smem_desc_sf(sfb_base + stage * kSfbBytes + h * 2048 + kk * 512));
-                }
-                tc_commit(&sf_ready[stage]);
-                if (++stage == kStages) { stage = 0; phase ^= 1; }
-            }
-        }
-        tc_commit(cp_done);
-        mbar_wait(cp_done, 0, p.err_flag, kErrTimeout, kWaitNs);
-    } else if (warp == 1 && lane == 0) {
-        // ----------------------------------------------------------- MMA --
-        int stage = 0;
-        uint32_t phase = 0, acc_phase = 0;
-        const uint32_t a_base = smem_u32(smem + kOffA);
-        const uint32_t b_base = smem_u32(smem + kOffB);
-        bool ok = true;
-        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-            const Tile t = tile_coord(tile, p.num_m_blk, p.num_n_blk);
-            const int n_rows = min(kBN, p.n_out - t.nb * kBN);
-            const uint32_t idesc = n_rows > 128 ? idesc_nvf4(128, 256) : idesc_nvf4(128, 128);
-            if (!mbar_wait(tmem_empty, acc_phase ^ 1, p.err_flag, kErrTimeout, kWaitNs)) break;
-            tc_fence_after_sync();
-            for (int ks = 0; ks < num_ks; ++ks) {
-                if (!mbar_wait(&sf_ready[stage], phase, p.err_flag, kErrTimeout, kWaitNs) ||
-                    !mbar_wait(&full[stage], phase, p.err_flag, kErrTimeout, kWaitNs)) { ok = false; break; }
-                tc_fence_after_sync();
-                const int kcount = min(4, p.num_k64 - ks * 4);
-                const uint32_t sf_col = tmem + kTmemSf + stage * kSfColsPerStage;
-                const uint64_t adesc = smem_desc_sw128(a_base + stage * kABytes);
-                const uint64_t bdesc = smem_desc_sw128(b_base + stage * kBBytes);
-                for (int kk = 0; kk < kcount; ++kk) {
-                    // K-step kk starts 32 bytes further into the swizzled 128-byte rows
-                    tc_mma_nvf4(tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc,
-                                sf_col + kk * 4, sf_col + 16 + kk * 8, (ks | kk) != 0);
-                }
-                tc_commit(&empty[stage]);
-                if (++stage == kStages) { stage = 0; phase ^= 1; }
-            }
-            if (!ok) break;
-            tc_commit(tmem_full);
-            acc_phase ^= 1;
-        }
-        // No MMA may still be running when the TMEM is released.
-        tc_commit(mma_done);
-        mbar_wait(mma_done, 0, p.err_flag, kErrTimeout, kWaitNs);
-    } else if (warp >= kEpiWarp0) {
+    if (threadIdx.x == 0) griddep_launch_dependents();   // the split-K reduce may get resident
+
+    // Roles by warpgroup; each warpgroup first resizes its register file.
+    if (warp >= kEpiWarp0) {
+        setmaxnreg_inc<kRegsEpi>();
         // ------------------------------------------------------ epilogue --
-        // Drain the whole 128 x 256 accumulator into registers as packed bf16
-        // (alpha and bias applied), release the TMEM to the MMA thread, and only
-        // then write the tile out, so the stores overlap the next tile's MMAs.
+        // Drain the finished 128 x 256 accumulator (this warp: TMEM lane
+        // quarter warp % 4, one row per thread) into registers as packed bf16
+        // with alpha and bias applied, hand the TMEM back to the MMA thread,
+        // then store the rows (rows < m, columns < n_out) while the next
+        // tile's MMAs run.  With split-K the drain writes raw fp32 sums.
         const int q = warp & 3;
-        uint16_t *s_bias = reinterpret_cast<uint16_t *>(smem + kOffBias) + (warp - kEpiWarp0) * kBN;
+        const uint32_t acc = tmem + ((uint32_t)(q * 32) << 16);
+        const uint32_t out_stage = smem_u32(smem + kOffOut) + (warp - kEpiWarp0) * 2 * kOutChunkBytes;
+        const bool use_bias = p.splits == 1 && p.bias != nullptr;
         const float alpha = __ldg(p.alpha);
         uint32_t acc_phase = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-            const Tile t = tile_coord(tile, p.num_m_blk, p.num_n_blk);
+        int it = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+            const Work wk = work_of(tile, p, num_ks);
+            const Tile t = wk.t;
             const int n_rows = min(kBN, p.n_out - t.nb * kBN);
             const int col_base = t.nb * kBN;
-            if (p.bias != nullptr) {                            // this warp's copy of the tile's bias
-                __syncwarp();                                   // previous tile done reading it
-                for (int j = lane; j < kBN; j += 32)
-                    s_bias[j] = (j < n_rows) ? p.bias[col_base + j] : (uint16_t)0;
-                __syncwarp();
-            }
-            if (!mbar_wait(tmem_full, acc_phase, p.err_flag, kErrTimeout, kWaitNs)) break;
+            const uint16_t *s_bias = reinterpret_cast<const uint16_t *>(smem + kOffBias) + (it & 1) * kBN;
+            if (use_bias &&
+                !__all_sync(~0u, mbar_wait(&bias_full[it & 1], (it >> 1) & 1, p.err_flag, kErrTimeout, kWaitNs)))
+                break;
+            if (!__all_sync(~0u, mbar_wait(tmem_full, acc_phase, p.err_flag, kErrTimeout, kWaitNs))) break;
             tc_fence_after_sync();
+            acc_phase ^= 1;
+            const int64_t row = (int64_t)t.mb * kBM + q * 32 + lane;
+            uint32_t r0[32], r1[32];
+
+            if (p.splits > 1) {
+                // split-K: raw fp32 sums of this K range for rows < m
+                float *dst = p.partials + ((int64_t)wk.split * p.m + row) * p.part_ld + col_base;
+                tmem_ld_32cols(acc, r0);
+#pragma unroll
+                for (int ch = 0; ch < kBN / 32; ++ch) {
+                    uint32_t(&cur)[32] = (ch & 1) ? r1 : r0;
+                    uint32_t(&nxt)[32] = (ch & 1) ? r0 : r1;
+                    if (ch * 32 < n_rows) {                     // uniform across the warp
+                        tmem_ld_wait_regs(cur);
+                        if (ch + 1 < kBN / 32 && (ch + 1) * 32 < n_rows) tmem_ld_32cols(acc + (ch + 1) * 32, nxt);
+                        if (row < p.m) {
+#pragma unroll
+                            for (int v = 0; v < 8; ++v)
+                                *reinterpret_cast<uint4 *>(dst + ch * 32 + 4 * v) =
+                                    make_uint4(cur[4 * v], cur[4 * v + 1], cur[4 * v + 2], cur[4 * v + 3]);
+                        }
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tmem_empty);
+                continue;
+            }
+
             uint32_t packed[kBN / 2];
+            tmem_ld_32cols(acc, r0);
 #pragma unroll
             for (int ch = 0; ch < kBN / 32; ++ch) {
+                uint32_t(&cur)[32] = (ch & 1) ? r1 : r0;
+                uint32_t(&nxt)[32] = (ch & 1) ? r0 : r1;
                 if (ch * 32 < n_rows) {                         // uniform across the warp
-                    uint32_t r[32];
-                    tmem_ld_32cols(tmem + ((uint32_t)(q * 32) << 16) + ch * 32, r);
-                    tmem_ld_wait();
+                    tmem_ld_wait_regs(cur);
+                    if (ch + 1 < kBN / 32 && (ch + 1) * 32 < n_rows) tmem_ld_32cols(acc + (ch + 1) * 32, nxt);
 #pragma unroll
                     for (int j = 0; j < 32; j += 2) {
                         float b0 = 0.0f, b1 = 0.0f;
-                        if (p.bias != nullptr) {
+                        if (use_bias) {
                             const uint32_t bw = *reinterpret_cast<const uint32_t *>(s_bias + ch * 32 + j);
                             b0 = __uint_as_float(bw << 16);
                             b1 = __uint_as_float(bw & 0xFFFF0000u);
                         }
-                        const uint32_t lo = bf16_bits_rn(__fmaf_rn(__uint_as_float(r[j]), alpha, b0));
-                        const uint32_t hi = bf16_bits_rn(__fmaf_rn(__uint_as_float(r[j + 1]), alpha, b1));
-                        packed[ch * 16 + j / 2] = lo | (hi << 16);
+                        packed[ch * 16 + j / 2] = bf16x2_rn(__fmaf_rn(__uint_as_float(cur[j]), alpha, b0),
+                                                            __fmaf_rn(__uint_as_float(cur[j + 1]), alpha, b1));
                     }
                 }
             }
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tmem_empty);
-            acc_phase ^= 1;
+            if (lane == 0) {
+                mbar_arrive(tmem_empty);
+                if (use_bias) mbar_arrive(&bias_empty[it & 1]);
+            }
 
-            const int64_t row = (int64_t)t.mb * kBM + q * 32 + lane;
-            if (row < p.m) {
-                uint16_t *orow = p.out + row * p.ldo + col_base;
+            // Store through shared memory and the TMA: 16-column chunks of this
+            // warp's 32 rows, two staging buffers; the TMA clips rows >= m and
+            // columns >= n_out.  (Thread-per-row global stores would touch 32
+            // rows per instruction and congest the SM's memory pipeline that
+            // the MMA thread's barrier and issue traffic also uses.)
+            const int row0 = t.mb * kBM + q * 32;
 #pragma unroll
-                for (int v = 0; v < kBN / 8; ++v) {
-                    if (v * 8 + 8 <= n_rows) {
-                        *reinterpret_cast<uint4 *>(orow + v * 8) =
-                            make_uint4(packed[v * 4], packed[v * 4 + 1], packed[v * 4 + 2], packed[v * 4 + 3]);
-                    } else if (v * 8 < n_rows) {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            if (v * 8 + e < n_rows)
-                                orow[v * 8 + e] = (uint16_t)(packed[v * 4 + e / 2] >> ((e & 1) * 16));
+            for (int c = 0; c < kBN / 16; ++c) {
+                if (c * 16 < n_rows) {                          // uniform across the warp
+                    const uint32_t buf = out_stage + (c & 1) * kOutChunkBytes;
+                    if (lane == 0) bulk_wait_group_read<1>();   // the store that last read `buf` is done with it
+                    __syncwarp();
+                    st_shared_v4(buf + lane * 32, packed[c * 8], packed[c * 8 + 1], packed[c * 8 + 2],
+                                 packed[c * 8 + 3]);
+                    st_shared_v4(buf + lane * 32 + 16, packed[c * 8 + 4], packed[c * 8 + 5], packed[c * 8 + 6],
+                                 packed[c * 8 + 7]);
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmOut, buf, col_base + c * 16, row0);
+                        bulk_commit_group();
                     }
                 }
             }
+        }
+        if (lane == 0) bulk_wait_group<0>();                    // all output written before the CTA exits
+    } else if (warp >= kSfWarp0) {
+        setmaxnreg_dec<kRegsSf>();
+        // ----------------------------------------------- scale staging --
+        // When a stage lands, copy its scale tiles from shared memory into the
+        // stage's TMEM columns with tcgen05.st (the tensor pipe's tcgen05.cp
+        // would queue behind the MMAs) and arrive on sf_ready[stage].  The
+        // tcgen05.cp 32x128b.warpx4 layout is reproduced: lane 32q + i of
+        // the quarter q gets bytes [16i, 16i + 16) of each 512-byte tile.
+        // A stage's columns are rewritten only after it landed again, i.e.
+        // after the MMAs that read them completed and released the stage.
+        const int q = warp & 3;
+        const uint32_t sf_tmem = tmem + ((uint32_t)(q * 32) << 16) + kTmemSf;
+        const uint32_t sfa_smem = smem_u32(smem + kOffSfa) + lane * 16;
+        const uint32_t sfb_smem = smem_u32(smem + kOffSfb) + lane * 16;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            const Work wk = work_of(tile, p, num_ks);
+            for (int ks = wk.ks0; ks < wk.ks1; ++ks) {
+                ok = __all_sync(~0u, mbar_wait(&full[stage], phase, p.err_flag, kErrTimeout, kWaitNs));
+                if (!ok) break;
+                uint32_t a[16], b[32];
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint4 v = ld_shared_v4(sfa_smem + stage * kSfaBytes + kk * 512);
+                    a[kk * 4 + 0] = v.x; a[kk * 4 + 1] = v.y; a[kk * 4 + 2] = v.z; a[kk * 4 + 3] = v.w;
+                }
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint4 v = ld_shared_v4(sfb_smem + stage * kSfbBytes + h * 2048 + kk * 512);
+                        uint32_t *d = b + kk * 8 + h * 4;
+                        d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
+                    }
+                // (tiles past the valid K-steps or B rows hold stale bytes; the
+                // MMAs never read their columns)
+                tmem_st_16cols(sf_tmem + stage * kSfColsPerStage, a);
+                tmem_st_32cols(sf_tmem + stage * kSfColsPerStage + 16, b);
+                tmem_st_wait();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sf_ready[stage]);
+                if (++stage == kStages) { stage = 0; phase ^= 1; }
+            }
+        }
+    } else {
+        setmaxnreg_dec<kRegsCtl>();
+        if (warp == 0 && lane == 0) {
+            // ------------------------------------------------------ producer --
+            const uint64_t pol_a = l2_policy_evict_last();
+            const uint64_t pol_b = l2_policy_evict_last();
+            // Weight side (B tile and its scale tiles) of one stage fill; arms
+            // the stage's barrier with the bytes of the whole fill.
+            auto issue_w = [&](int stage, const Work &wk, int ks) {
+                const Tile t = wk.t;
+                const int halves = min(kBN, p.n_out - t.nb * kBN) > 128 ? 2 : 1;
+                const uint32_t sf_bytes = (uint32_t)min(4, p.num_k64 - ks * 4) * 512;
+                mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes + sf_bytes * (1 + halves));
+                tma_load_2d(smem + kOffB + stage * kBBytes, &tmB, &full[stage], ks * kBKBytes, t.nb * kBN, pol_b);
+                for (int h = 0; h < halves; ++h)        // halves == 2 implies band t.nb*2+1 exists
+                    bulk_load(smem + kOffSfb + stage * kSfbBytes + h * 2048,
+                              p.sfb + (t.nb * 2 + h) * p.sfb_band_bytes + (int64_t)ks * 2048, sf_bytes, &full[stage],
+                              pol_b);
+            };
+            // Activation side (A tile and its scale tile) of the same fill.
+            auto issue_a = [&](int stage, const Work &wk, int ks) {
+                const uint32_t sf_bytes = (uint32_t)min(4, p.num_k64 - ks * 4) * 512;
+                tma_load_2d(smem + kOffA + stage * kABytes, &tmA, &full[stage], ks * kBKBytes, wk.t.mb * kBM, pol_a);
+                bulk_load(smem + kOffSfa + stage * kSfaBytes, p.sfa + wk.t.mb * p.sfa_band_bytes + (int64_t)ks * 2048,
+                          sf_bytes, &full[stage], pol_a);
+            };
+            // The first kStages fills start with their weight side, before the
+            // wait for the preceding grid: launched as the dependent of the
+            // activation quantizer, the GEMM streams weights (which that grid
+            // does not write) while the quantizer is still running.
+            int pre = 0;
+            for (int tile = blockIdx.x; tile < num_tiles && pre < kStages; tile += gridDim.x) {
+                const Work wk = work_of(tile, p, num_ks);
+                for (int ks = wk.ks0; ks < wk.ks1 && pre < kStages; ++ks) issue_w(pre++, wk, ks);
+            }
+            griddep_wait();
+            int stage = 0, fill = 0;
+            uint32_t phase = 0;
+            uint32_t issued_mask = 0, issued_phase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+                const Work wk = work_of(tile, p, num_ks);
+                for (int ks = wk.ks0; ks < wk.ks1; ++ks, ++fill) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1, p.err_flag, kErrTimeout, kWaitNs)) { ok = false; break; }
+                    if (fill >= pre) issue_w(stage, wk, ks);
+                    issue_a(stage, wk, ks);
+                    issued_mask |= 1u << stage;
+                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == kStages) { stage = 0; phase ^= 1; }
+                }
+            }
+            (void)n_bands_w;
+            // Every copy this thread issued has landed before the CTA may exit.
+            // (The pre-issued fills pass the loop above before any wait that can
+            // time out: their empty barriers are fresh.)
+            for (int s = 0; s < kStages; ++s)
+                if (issued_mask & (1u << s))
+                    mbar_wait(&full[s], (issued_phase >> s) & 1u, p.err_flag, kErrTimeout, kWaitNs);
+        } else if (warp == 2 && p.splits == 1 && p.bias != nullptr) {
+            // ---------------------------------------------------- bias loader --
+            // The bias of each tile into one of two shared buffers, for the
+            // four epilogue warps (bias_full / bias_empty per buffer).
+            uint16_t *s_bias_all = reinterpret_cast<uint16_t *>(smem + kOffBias);
+            int it = 0;
+            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+                const Tile t = work_of(tile, p, num_ks).t;
+                const int n_rows = min(kBN, p.n_out - t.nb * kBN);
+                const int b = it & 1;
+                if (!__all_sync(~0u, mbar_wait(&bias_empty[b], ((it >> 1) & 1) ^ 1, p.err_flag, kErrTimeout,
+                                               kWaitNs)))
+                    break;
+                for (int j = lane; j < kBN; j += 32)
+                    s_bias_all[b * kBN + j] = (j < n_rows) ? p.bias[t.nb * kBN + j] : (uint16_t)0;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bias_full[b]);
+            }
+        } else if (warp == 1 && lane == 0) {
+            // ----------------------------------------------------------- MMA --
+            int stage = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            const uint32_t a_base = smem_u32(smem + kOffA);
+            const uint32_t b_base = smem_u32(smem + kOffB);
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+                const Work wk = work_of(tile, p, num_ks);
+                const int n_rows = min(kBN, p.n_out - wk.t.nb * kBN);
+                const uint32_t idesc = n_rows > 128 ? idesc_nvf4(128, 256) : idesc_nvf4(128, 128);
+                if (!mbar_wait(tmem_empty, acc_phase ^ 1, p.err_flag, kErrTimeout, kWaitNs)) break;
+                tc_fence_after_sync();
+                for (int ks = wk.ks0; ks < wk.ks1; ++ks) {
+                    if (!mbar_wait(&sf_ready[stage], phase, p.err_flag, kErrTimeout, kWaitNs) ||
+                        !mbar_wait(&full[stage], phase, p.err_flag, kErrTimeout, kWaitNs)) { ok = false; break; }
+                    tc_fence_after_sync();
+                    const int kcount = min(4, p.num_k64 - ks * 4);
+                    const uint32_t sf_col = tmem + kTmemSf + stage * kSfColsPerStage;
+                    const uint64_t adesc = smem_desc_sw128(a_base + stage * kABytes);
+                    const uint64_t bdesc = smem_desc_sw128(b_base + stage * kBBytes);
+                    for (int kk = 0; kk < kcount; ++kk) {
+                        // K-step kk starts 32 bytes further into the swizzled 128-byte rows
+                        tc_mma_nvf4(tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc,
+                                    sf_col + kk * 4, sf_col + 16 + kk * 8, (ks != wk.ks0 || kk != 0));
+                    }
+                    tc_commit(&empty[stage]);
+                    if (++stage == kStages) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                tc_commit(tmem_full);
+                acc_phase ^= 1;
+            }
+            // No MMA may still be running when the TMEM is released.
+            tc_commit(mma_done);
+            mbar_wait(mma_done, 0, p.err_flag, kErrTimeout, kWaitNs);
         }
     }
 
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
-    if (warp == 2) tmem_dealloc(tmem, kTmemCols);
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// Split-K finish: out[r, c] = bf16(alpha * sum_s partials[s][r][c] + bias[c])
+// for r < m, c < n_out, the splits summed in index order (deterministic).
+// Each thread handles four consecutive columns.
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const GemmParams p)
+{
+    griddep_wait();                                 // the split GEMM's partials are complete
+    const float alpha = __ldg(p.alpha);
+    const int groups = (p.n_out + 3) / 4;
+    const int64_t total = (int64_t)p.m * groups;
+    const int64_t split_stride = (int64_t)p.m * p.part_ld;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / groups;
+        const int c = (int)(i - r * groups) * 4;
+        const float *src = p.partials + r * p.part_ld + c;
+        // all loads in flight at once, then the sum in split order
+        float4 v[kMaxSplits];
+#pragma unroll
+        for (int sp = 0; sp < kMaxSplits; ++sp)
+            if (sp < p.splits) v[sp] = __ldcs(reinterpret_cast<const float4 *>(src + sp * split_stride));
+        float4 acc = v[0];
+#pragma unroll
+        for (int sp = 1; sp < kMaxSplits; ++sp)
+            if (sp < p.splits) { acc.x += v[sp].x; acc.y += v[sp].y; acc.z += v[sp].z; acc.w += v[sp].w; }
+        const float a[4] = {acc.x, acc.y, acc.z, acc.w};
+        uint16_t *o = p.out + r * p.ldo + c;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (c + e < p.n_out) {
+                const float b = p.bias ? __uint_as_float((uint32_t)p.bias[c + e] << 16) : 0.0f;
+                o[e] = (uint16_t)bf16_bits_rn(__fmaf_rn(a[e], alpha, b));
+            }
+    }
 }
 
 }  // namespace
 
+cudaError_t launch_splitk_reduce(const GemmParams &p, int num_sms, cudaStream_t s)
+{
+    const int64_t total = (int64_t)p.m * ((p.n_out + 3) / 4);
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > (int64_t)num_sms * 8) blocks = (int64_t)num_sms * 8;
+    if (blocks < 1) blocks = 1;
+    if (p.splits < 2 || p.splits > kMaxSplits) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = s;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, p);
+}
+
 cudaError_t launch_gemm(const GemmParams &p, const uint8_t *a, const uint8_t *w, int num_sms, cudaStream_t s,
-                        const char **why)
+                        const char **why, bool dependent)
 {
     static int configured_device = -1;
     int dev = 0;
@@ -318,17 +499,34 @@ cudaError_t launch_gemm(const GemmParams &p, const uint8_t *a, const uint8_t *w,
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    CUtensorMap tmA, tmB;
+    CUtensorMap tmA, tmB, tmOut;
     const uint64_t row_bytes = (uint64_t)p.kp / 2;
     if (!make_operand_map(&tmA, a, row_bytes, (uint64_t)p.m, kBM) ||
         !make_operand_map(&tmB, w, row_bytes, (uint64_t)p.n_w, kBN)) {
         *why = "cuTensorMapEncodeTiled failed for an FP4 operand";
         return cudaErrorInvalidValue;
     }
-    const int tiles = p.num_m_blk * p.num_n_blk;
+    if (p.splits == 1) {
+        if (!make_output_map(&tmOut, p.out, (uint64_t)p.n_out, (uint64_t)p.m, (uint64_t)p.ldo)) {
+            *why = "cuTensorMapEncodeTiled failed for the output";
+            return cudaErrorInvalidValue;
+        }
+    } else {
+        tmOut = tmA;                                    // not used: split-K writes partial sums
+    }
+    const int tiles = p.num_m_blk * p.num_n_blk * p.splits;
     const int grid = tiles < num_sms ? tiles : num_sms;
-    gemm_nvf4_kernel<<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cfg.attrs = dependent ? &attr : nullptr;
+    cfg.numAttrs = dependent ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, gemm_nvf4_kernel, tmA, tmB, tmOut, p);
 }
 
 }  // namespace nvfp4

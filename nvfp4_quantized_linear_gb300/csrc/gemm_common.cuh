@@ -49,21 +49,39 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
     return fn;
 }
 
-// 2-D map over a packed FP4 operand [rows, row_bytes] with 128-byte-wide boxes
-// of `box_rows` rows, 128-byte swizzle, zero fill outside the tensor.
-inline bool make_operand_map(CUtensorMap *map, const void *base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows)
+// 2-D map over a packed FP4 operand [rows, row_bytes] with boxes of
+// `box_bytes` (64 or 128) x `box_rows`, swizzled with the same width, zero
+// fill outside the tensor.
+inline bool make_operand_map(CUtensorMap *map, const void *base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows,
+                             uint32_t box_bytes = 128)
 {
     auto encode = tensor_map_encoder();
     if (encode == nullptr) return false;
     cuuint64_t dims[2] = {row_bytes, rows};
     cuuint64_t strides[1] = {row_bytes};
-    cuuint32_t box[2] = {128u, box_rows};
+    cuuint32_t box[2] = {box_bytes, box_rows};
     cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapSwizzle swz = box_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
     return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Map of the bf16 output [m, n_out] (row stride ldo elements) for TMA stores
+// of 16-column x 32-row boxes, no swizzle.  The TMA skips elements outside
+// [0, n_out) x [0, m).  Requires a 16-B aligned base and ldo % 8 == 0.
+inline bool make_output_map(CUtensorMap *map, void *base, uint64_t n_out, uint64_t m, uint64_t ldo)
+{
+    auto encode = tensor_map_encoder();
+    if (encode == nullptr) return false;
+    cuuint64_t dims[2] = {n_out, m};
+    cuuint64_t strides[1] = {ldo * 2};
+    cuuint32_t box[2] = {16, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 }  // namespace gemm_detail
 }  // namespace nvfp4

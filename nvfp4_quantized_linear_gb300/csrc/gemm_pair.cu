@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_commit_pair(mma_done);
         mbar_wait(mma_done, 0, p.err_flag, kErrTimeout, kWaitNs);
-    } else if (warp >= kEpiWarp0) {
+    } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiWarps) {
         // ------------------------------------------------------ epilogue --
         const int q = warp & 3;
         uint16_t *s_bias = reinterpret_cast<uint16_t *>(smem + kOffBias) + (warp - kEpiWarp0) * kTileN;

@@ -78,7 +78,7 @@ nvfp4_status nvfp4_linear_noalloc(const void *x_bf16, int64_t m, int64_t k, int6
     if (m == 0)   // an empty call needs no scratch; let the regular checks answer it
         return nvfp4_linear(x_bf16, m, k, ldx, gs_dev, transform_bf16, bs, w_fp4, w_sf, n_w, n_out, alpha_dev,
                             bias_bf16, out_bf16, ldo, nullptr, 0, stream);
-    const size_t need = nvfp4_linear_workspace_bytes(m, k, n_w);
+    const size_t need = nvfp4::linear_min_workspace_bytes(m, k);
     if (m < 0 || k < 1 || need > kScratchBytes) {
         char msg[200];
         snprintf(msg, sizeof msg,

@@ -90,6 +90,9 @@ __global__ void __launch_bounds__(256) quant_kernel(const QuantParams p)
     const int lane = threadIdx.x & 31;
     const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int nwarps = (int)((gridDim.x * blockDim.x) >> 5);
+    // A programmatic dependent (the GEMM of the linear layer) may start its
+    // prologue now; it waits for this grid before touching its data.
+    if (threadIdx.x == 0) griddep_launch_dependents();
     const float gs = __ldg(p.gs);
     const int segs = (p.kp + 511) >> 9;
     const int tasks = p.mp * segs;                    // < 2^31: checked on the host
@@ -153,6 +156,7 @@ __global__ void __launch_bounds__(256) quant_transform_kernel(const QuantParams 
     float *sT = smem_f;
     uint32_t *sX = reinterpret_cast<uint32_t *>(smem_f + bs * bs);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) griddep_launch_dependents();    // as in quant_kernel
 
     for (int i = tid; i < bs * bs; i += 256) sT[i] = __uint_as_float((uint32_t)p.t[i] << 16);
     const float gs = __ldg(p.gs);

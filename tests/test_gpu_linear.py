@@ -106,3 +106,52 @@ def test_linear_rejects_small_workspace():
         nv.nvfp4_linear(x, 4, 64, 64, dev_scalar(1.0), None, 0, w_fp4, w_sf, 128, 128, dev_scalar(1.0), None,
                         out, 128, ws, 16)
     assert e.value.status == 7
+
+
+SPLIT_K = [syn.Problem("splitk", f"m{m}-n{n}-k{k}", m, k, n, seed=1300 + i, bias=bias, n_out=n_out)
+           for i, (m, k, n, n_out, bias) in enumerate([
+               (1, 4096, 256, None, False),      # one output tile: 16 splits of 4 stages
+               (5, 4104, 1024, 1000, True),      # ragged K (65 k-steps), sliced output, bias
+               (64, 14336, 4096, None, True),    # Llama down_proj width at decode size
+               (128, 2048, 512, 500, False),     # full band, 2 tiles
+               (33, 64, 256, None, True),        # a single K stage: no split
+           ])]
+
+
+@pytest.mark.parametrize("p", SPLIT_K, ids=_ids(SPLIT_K))
+def test_split_k_matches_oracle_and_unsplit(p):
+    """Small m with the full workspace takes the split-K path (fp32 partials +
+    ordered reduce); it must match the oracle on every element, agree with the
+    unsplit GEMM (minimum workspace) to fp32-summation-order accuracy, and be
+    bit-identical across calls."""
+    L = syn.make_layer(p, device="cuda")
+    m, k, n_out = p.m, p.k, p.n_keep
+    w_fp4, w_sf = nv.prepare_weight(L.w, dev_scalar(L.gs_w))
+    gs, alpha = dev_scalar(L.gs_x), dev_scalar(L.alpha)
+    full = nv.nvfp4_linear_workspace_bytes(m, k, p.n)
+    small = (nv.nvfp4_packed_bytes(m, k) + 255) // 256 * 256 + (nv.nvfp4_scale_bytes(m, k) + 255) // 256 * 256
+    assert full > small
+    outs = []
+    for ws_bytes in (full, full, small):
+        ws = torch.full((ws_bytes,), 0xA5, dtype=torch.uint8, device="cuda")
+        ldo = (n_out + 7) // 8 * 8                       # output rows 16-byte aligned
+        out = torch.full((m, ldo), float("nan"), dtype=torch.bfloat16, device="cuda")[:, :n_out]
+        nv.nvfp4_linear(L.x, m, k, L.x.stride(0), gs, None, 0, w_fp4, w_sf, p.n, n_out, alpha, L.bias,
+                        out, out.stride(0), ws, ws_bytes)
+        torch.cuda.synchronize()
+        nv.nvfp4_device_error()
+        outs.append(out)
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16)), "split-K not deterministic"
+    a, sa = oracle.quantize(syn.bf16_bits(L.x), L.gs_x, k=k)
+    b, sb = oracle.quantize(syn.bf16_bits(L.w[:n_out]), L.gs_w, k=k)
+    bias = syn.bf16_bits(L.bias[:n_out]) if L.bias is not None else None
+    ref = oracle.gemm(a, sa, b, sb, L.alpha, bias)
+    assert_gemm_close(bf16_to_f64(outs[0]), ref, f"split-K {p.name}")
+    assert_gemm_close(bf16_to_f64(outs[2]), ref, f"unsplit {p.name}")
+    split, unsplit = bf16_to_f64(outs[0]), bf16_to_f64(outs[2])
+    # The fp32 sums differ only in order (a few fp32 ulp of the summed terms),
+    # so after the bf16 rounding the two differ by at most one bf16 ulp
+    # (2^-7 relative) plus that fp32 noise.
+    rms = np.sqrt(np.mean(ref ** 2))
+    bound = 2.0 ** -7 * np.maximum(np.abs(split), np.abs(unsplit)) + 1e-5 * rms
+    assert np.all(np.abs(split - unsplit) <= bound), "split-K and unsplit GEMM differ beyond rounding"
