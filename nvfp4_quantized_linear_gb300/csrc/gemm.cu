@@ -7,7 +7,7 @@
 //     out[m, n] = bf16( alpha * sum_k A[m,k] B[n,k] + bias[n] ),  n < n_out,
 // A, B packed E2M1 (K-major) with one UE4M3 scale per 16 K-elements.
 //
-// Design (one CTA per SM, persistent over output tiles of 128 x 256; 12 warps):
+// Design (one CTA per SM, persistent over output tiles of 128 x 256; 16 warps):
 //   warp 0      TMA producer: A tile 128 x 256 FP4 (16 KB), B tile 256 x 256 FP4
 //               (32 KB), both 128-byte swizzled, plus the matching 512-byte
 //               scale tiles by bulk copy, into a 4-stage shared-memory ring.
@@ -20,8 +20,8 @@
 //   warps 4..7  one per TMEM lane quarter: stage each landed stage's scale
 //               tiles into TMEM with tcgen05.st, keeping the tensor pipe for
 //               the MMAs alone;
-//   warps 8..11 epilogue, one per TMEM lane quarter: tcgen05.ld of finished
-//               accumulators, fma with alpha and bias, bf16 round into
+//   warps 8..15 epilogue, two per TMEM lane quarter (128 columns each):
+//               tcgen05.ld of finished accumulators, fma with alpha and bias, bf16 round into
 //               registers, release of the TMEM tile, then masked stores
 //               (rows < m, cols < n_out) that overlap the next tile's MMAs.
 //               With split-K the drain writes raw fp32 partial sums instead.
@@ -65,21 +65,22 @@ constexpr uint32_t kOffSfa = kOffB + kStages * kBBytes;
 constexpr uint32_t kOffSfb = kOffSfa + kStages * kSfaBytes;
 constexpr uint32_t kOffBias = kOffSfb + kStages * kSfbBytes;   // two tiles of bias (bf16), double-buffered
 constexpr uint32_t kOutChunkBytes = 32 * 16 * 2;              // output staging: 32 rows x 16 columns bf16
-constexpr uint32_t kOffOut = kOffBias + 2 * kBN * 2;          // per epilogue warp: two staging chunks
-constexpr uint32_t kOffBar = kOffOut + 4 * 2 * kOutChunkBytes;
+constexpr uint32_t kOffOut = kOffBias + 2 * kBN * 2;          // per epilogue warp: one staging chunk
+constexpr uint32_t kOffBar = kOffOut + 8 * kOutChunkBytes;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;   // barriers + alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemSf = 256;
 constexpr uint32_t kSfColsPerStage = 48;
 constexpr uint64_t kWaitNs = 2000000000ull;
-constexpr int kThreads = 384;                 // three warpgroups
+constexpr int kThreads = 512;                 // four warpgroups
 constexpr int kSfWarp0 = 4;                   // warps 4..7: scale staging, lane quarter warp % 4
-constexpr int kEpiWarp0 = 8;                  // warps 8..11: epilogue, lane quarter warp % 4
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarp0 = 8;                  // warps 8..15: epilogue, lane quarter warp % 4,
+constexpr int kEpiWarps = 8;                  // columns [128 h, 128 h + 128) for h = (warp - 8) / 4
+constexpr int kEpiCols = kBN / 2;
 // Registers per thread after the reallocation at kernel start (launched with
-// 65536 / 384 = 168): 128 x (56 + 96 + 240) = 50176 <= 384 x 168 = 64512.
-constexpr uint32_t kRegsCtl = 56, kRegsSf = 96, kRegsEpi = 240;
-static_assert(128 * (kRegsCtl + kRegsSf + kRegsEpi) <= kThreads * 168, "register reallocation budget");
+// 65536 / 512 = 128): 128 x (56 + 96 + 2 x 176) = 64512 <= 512 x 128 = 65536.
+constexpr uint32_t kRegsCtl = 56, kRegsSf = 96, kRegsEpi = 176;
+static_assert(128 * (kRegsCtl + kRegsSf + 2 * kRegsEpi) <= kThreads * 128, "register reallocation budget");
 
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffOut % 128 == 0, "TMA store sources are 128-byte aligned");
@@ -162,8 +163,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // then store the rows (rows < m, columns < n_out) while the next
         // tile's MMAs run.  With split-K the drain writes raw fp32 sums.
         const int q = warp & 3;
-        const uint32_t acc = tmem + ((uint32_t)(q * 32) << 16);
-        const uint32_t out_stage = smem_u32(smem + kOffOut) + (warp - kEpiWarp0) * 2 * kOutChunkBytes;
+        const int hcol = ((warp - kEpiWarp0) >> 2) * kEpiCols;    // this warp's first column of the tile
+        const uint32_t acc = tmem + ((uint32_t)(q * 32) << 16) + hcol;
+        const uint32_t out_stage = smem_u32(smem + kOffOut) + (warp - kEpiWarp0) * kOutChunkBytes;
         const bool use_bias = p.splits == 1 && p.bias != nullptr;
         const float alpha = __ldg(p.alpha);
         uint32_t acc_phase = 0;
@@ -171,9 +173,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
             const Work wk = work_of(tile, p, num_ks);
             const Tile t = wk.t;
-            const int n_rows = min(kBN, p.n_out - t.nb * kBN);
-            const int col_base = t.nb * kBN;
-            const uint16_t *s_bias = reinterpret_cast<const uint16_t *>(smem + kOffBias) + (it & 1) * kBN;
+            const int n_cols = min(kEpiCols, p.n_out - t.nb * kBN - hcol);   // may be <= 0
+            const int col_base = t.nb * kBN + hcol;
+            const uint16_t *s_bias = reinterpret_cast<const uint16_t *>(smem + kOffBias) + (it & 1) * kBN + hcol;
             if (use_bias &&
                 !__all_sync(~0u, mbar_wait(&bias_full[it & 1], (it >> 1) & 1, p.err_flag, kErrTimeout, kWaitNs)))
                 break;
@@ -186,14 +188,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (p.splits > 1) {
                 // split-K: raw fp32 sums of this K range for rows < m
                 float *dst = p.partials + ((int64_t)wk.split * p.m + row) * p.part_ld + col_base;
-                tmem_ld_32cols(acc, r0);
+                if (n_cols > 0) tmem_ld_32cols(acc, r0);
 #pragma unroll
-                for (int ch = 0; ch < kBN / 32; ++ch) {
+                for (int ch = 0; ch < kEpiCols / 32; ++ch) {
                     uint32_t(&cur)[32] = (ch & 1) ? r1 : r0;
                     uint32_t(&nxt)[32] = (ch & 1) ? r0 : r1;
-                    if (ch * 32 < n_rows) {                     // uniform across the warp
+                    if (ch * 32 < n_cols) {                     // uniform across the warp
                         tmem_ld_wait_regs(cur);
-                        if (ch + 1 < kBN / 32 && (ch + 1) * 32 < n_rows) tmem_ld_32cols(acc + (ch + 1) * 32, nxt);
+                        if (ch + 1 < kEpiCols / 32 && (ch + 1) * 32 < n_cols)
+                            tmem_ld_32cols(acc + (ch + 1) * 32, nxt);
                         if (row < p.m) {
 #pragma unroll
                             for (int v = 0; v < 8; ++v)
@@ -208,15 +211,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 continue;
             }
 
-            uint32_t packed[kBN / 2];
-            tmem_ld_32cols(acc, r0);
+            uint32_t packed[kEpiCols / 2];
+            if (n_cols > 0) tmem_ld_32cols(acc, r0);
 #pragma unroll
-            for (int ch = 0; ch < kBN / 32; ++ch) {
+            for (int ch = 0; ch < kEpiCols / 32; ++ch) {
                 uint32_t(&cur)[32] = (ch & 1) ? r1 : r0;
                 uint32_t(&nxt)[32] = (ch & 1) ? r0 : r1;
-                if (ch * 32 < n_rows) {                         // uniform across the warp
+                if (ch * 32 < n_cols) {                         // uniform across the warp
                     tmem_ld_wait_regs(cur);
-                    if (ch + 1 < kBN / 32 && (ch + 1) * 32 < n_rows) tmem_ld_32cols(acc + (ch + 1) * 32, nxt);
+                    if (ch + 1 < kEpiCols / 32 && (ch + 1) * 32 < n_cols) tmem_ld_32cols(acc + (ch + 1) * 32, nxt);
 #pragma unroll
                     for (int j = 0; j < 32; j += 2) {
                         float b0 = 0.0f, b1 = 0.0f;
@@ -238,25 +241,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 
             // Store through shared memory and the TMA: 16-column chunks of this
-            // warp's 32 rows, two staging buffers; the TMA clips rows >= m and
+            // warp's 32 rows x 128 columns; the TMA clips rows >= m and
             // columns >= n_out.  (Thread-per-row global stores would touch 32
             // rows per instruction and congest the SM's memory pipeline that
             // the MMA thread's barrier and issue traffic also uses.)
             const int row0 = t.mb * kBM + q * 32;
 #pragma unroll
-            for (int c = 0; c < kBN / 16; ++c) {
-                if (c * 16 < n_rows) {                          // uniform across the warp
-                    const uint32_t buf = out_stage + (c & 1) * kOutChunkBytes;
-                    if (lane == 0) bulk_wait_group_read<1>();   // the store that last read `buf` is done with it
+            for (int c = 0; c < kEpiCols / 16; ++c) {
+                if (c * 16 < n_cols) {                          // uniform across the warp
+                    if (lane == 0) bulk_wait_group_read<0>();   // the previous chunk's store has read the buffer
                     __syncwarp();
-                    st_shared_v4(buf + lane * 32, packed[c * 8], packed[c * 8 + 1], packed[c * 8 + 2],
+                    st_shared_v4(out_stage + lane * 32, packed[c * 8], packed[c * 8 + 1], packed[c * 8 + 2],
                                  packed[c * 8 + 3]);
-                    st_shared_v4(buf + lane * 32 + 16, packed[c * 8 + 4], packed[c * 8 + 5], packed[c * 8 + 6],
-                                 packed[c * 8 + 7]);
+                    st_shared_v4(out_stage + lane * 32 + 16, packed[c * 8 + 4], packed[c * 8 + 5],
+                                 packed[c * 8 + 6], packed[c * 8 + 7]);
                     fence_proxy_async_shared();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&tmOut, buf, col_base + c * 16, row0);
+                        tma_store_2d(&tmOut, out_stage, col_base + c * 16, row0);
                         bulk_commit_group();
                     }
                 }
@@ -386,8 +388,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bias_full[b]);
             }
-        } else if (warp == 1 && lane == 0) {
+        } else if (warp == 1) {
             // ----------------------------------------------------------- MMA --
+            // The whole warp runs the loop, so every value in it stays
+            // warp-uniform; one elected lane issues the tcgen05 instructions
+            // (MMAs and the commits that track them).
+            const bool leader = elect_one();
             int stage = 0;
             uint32_t phase = 0, acc_phase = 0;
             const uint32_t a_base = smem_u32(smem + kOffA);
@@ -397,30 +403,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Work wk = work_of(tile, p, num_ks);
                 const int n_rows = min(kBN, p.n_out - wk.t.nb * kBN);
                 const uint32_t idesc = n_rows > 128 ? idesc_nvf4(128, 256) : idesc_nvf4(128, 128);
-                if (!mbar_wait(tmem_empty, acc_phase ^ 1, p.err_flag, kErrTimeout, kWaitNs)) break;
+                if (!__all_sync(~0u, mbar_wait(tmem_empty, acc_phase ^ 1, p.err_flag, kErrTimeout, kWaitNs))) break;
                 tc_fence_after_sync();
                 for (int ks = wk.ks0; ks < wk.ks1; ++ks) {
-                    if (!mbar_wait(&sf_ready[stage], phase, p.err_flag, kErrTimeout, kWaitNs) ||
-                        !mbar_wait(&full[stage], phase, p.err_flag, kErrTimeout, kWaitNs)) { ok = false; break; }
+                    // sf_ready implies full: the scale warps arrive on it only
+                    // after they saw the stage land (and read its scales).
+                    if (!__all_sync(~0u, mbar_wait(&sf_ready[stage], phase, p.err_flag, kErrTimeout, kWaitNs))) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after_sync();
                     const int kcount = min(4, p.num_k64 - ks * 4);
                     const uint32_t sf_col = tmem + kTmemSf + stage * kSfColsPerStage;
                     const uint64_t adesc = smem_desc_sw128(a_base + stage * kABytes);
                     const uint64_t bdesc = smem_desc_sw128(b_base + stage * kBBytes);
-                    for (int kk = 0; kk < kcount; ++kk) {
-                        // K-step kk starts 32 bytes further into the swizzled 128-byte rows
-                        tc_mma_nvf4(tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc,
-                                    sf_col + kk * 4, sf_col + 16 + kk * 8, (ks != wk.ks0 || kk != 0));
+                    if (leader) {
+                        for (int kk = 0; kk < kcount; ++kk) {
+                            // K-step kk starts 32 bytes further into the swizzled 128-byte rows
+                            tc_mma_nvf4(tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc,
+                                        sf_col + kk * 4, sf_col + 16 + kk * 8, (ks != wk.ks0 || kk != 0));
+                        }
+                        tc_commit(&empty[stage]);
                     }
-                    tc_commit(&empty[stage]);
                     if (++stage == kStages) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
-                tc_commit(tmem_full);
+                if (leader) tc_commit(tmem_full);
+                __syncwarp();
                 acc_phase ^= 1;
             }
             // No MMA may still be running when the TMEM is released.
-            tc_commit(mma_done);
+            if (leader) tc_commit(mma_done);
+            __syncwarp();
             mbar_wait(mma_done, 0, p.err_flag, kErrTimeout, kWaitNs);
         }
     }

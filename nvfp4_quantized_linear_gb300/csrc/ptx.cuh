@@ -301,6 +301,19 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi)
     return d;
 }
 
+// One lane of the (converged) warp gets true: the issuer of single-thread
+// tcgen05 instructions.  With a full member mask it is always the same lane.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t.reg .b32 R;\n\t"
+        "elect.sync R|P, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // Per-warpgroup register reallocation (all 128 threads of the warpgroup
 // execute it).  The increases of a block draw on what its decreases free, out
 // of the registers the block was launched with.
