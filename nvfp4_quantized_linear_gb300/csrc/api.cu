@@ -294,7 +294,7 @@ nvfp4_status run_gemm(const uint8_t *a, const uint8_t *a_sf, int64_t m, const ui
         }
     }
     const char *why = nullptr;
-    e = (m > 128 && g_use_pair_kernel) ? nvfp4::launch_gemm_pair(g, a, w, num_sms, s, &why)
+    e = (m > 128 && g_use_pair_kernel) ? nvfp4::launch_gemm_pair(g, a, w, num_sms, s, &why, after_quant)
                                        : nvfp4::launch_gemm(g, a, w, num_sms, s, &why, after_quant);
     if (why) return fail(NVFP4_ERR_CUDA, "%s", why);
     nvfp4_status st = launch_status(e, "GEMM kernel");

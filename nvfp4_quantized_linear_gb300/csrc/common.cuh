@@ -76,7 +76,7 @@ cudaError_t launch_gemm(const GemmParams &p, const uint8_t *a, const uint8_t *w,
 cudaError_t launch_splitk_reduce(const GemmParams &p, int num_sms, cudaStream_t s);
 // CTA-pair variant for m > 128 (tiles of 256 x 256 on two SMs).
 cudaError_t launch_gemm_pair(const GemmParams &p, const uint8_t *a, const uint8_t *w, int num_sms, cudaStream_t s,
-                             const char **why);
+                             const char **why, bool dependent = false);
 
 // Smallest workspace nvfp4_linear accepts: the quantized activation and its
 // scales (256-byte aligned inside); anything beyond it holds split-K partials.

@@ -2,21 +2,29 @@
 //
 // Same operation as gemm.cu (page "TorchNvFp4LinearKernel", vLLM PR #53319,
 // section 关键源码片段: _scaled_mm, * alpha, slice, + bias), with each output
-// tile of 256 x 256 computed by a cluster of two CTAs on two SMs:
-//   - CTA r (r = 0, 1) loads A rows [128r, 128r+128) of the tile and B rows
-//     [128r, 128r+128) of the tile (its half of N), plus the scale tiles of its
-//     A band and of both B bands, into a 5-stage shared-memory ring;
-//   - the leader CTA (r = 0) issues everything on the tensor cores for both:
-//     tcgen05.cp.cta_group::2 moves each CTA's scale tiles into that CTA's
-//     TMEM, tcgen05.mma.cta_group::2 (M=256, N=256, K=64) accumulates each
-//     CTA's 128 rows x 256 columns in that CTA's TMEM, and the commits
-//     multicast to both CTAs' barriers;
-//   - the peer CTA's copy completions reach the leader through a relay thread
-//     that arrives on a leader barrier at cluster scope;
-//   - each CTA's four epilogue warps drain its own accumulator, arrive on the
-//     leader's "accumulator free" barrier and store their rows.
-// Per SM and K-step this moves 8 KB of operand tiles instead of 12 KB, and the
-// scale copies and MMAs are issued once per pair.  Every mbarrier wait is
+// tile of 256 x 256 computed by a cluster of two CTAs on two SMs.  Per CTA
+// r (r = 0, 1; rank 0 leads), sixteen warps in four warpgroups:
+//   warp 0      TMA producer: this CTA's A rows [128r, 128r + 128) of the tile
+//               and its half of B (rows [128r, 128r + 128) of the tile's 256),
+//               plus the scale tiles of its A band and of both B bands (each
+//               CTA's TMEM needs the scales of all 256 B rows), into a 5-stage
+//               ring of 38 KB stages;
+//   warp 1      allocates the pair's TMEM; in the leader it issues, from one
+//               elected lane of the converged warp, tcgen05.mma.cta_group::2
+//               (M = 256, N = 256, K = 64): each CTA's tensor core reads its
+//               own A rows and both B halves and accumulates its 128 x 256
+//               fp32 tile in its own TMEM; the commits multicast to both CTAs'
+//               barriers;
+//   warp 2      loads each tile's bias into shared memory (two buffers);
+//   warps 4..7  stage each landed stage's scale tiles into this CTA's TMEM
+//               (tcgen05.st, one warp per lane quarter) and arrive on the
+//               leader's sf_ready[stage], which therefore completes once both
+//               CTAs' stages landed and both TMEMs hold their scales;
+//   warps 8..15 epilogue, two per TMEM lane quarter: drain this CTA's
+//               accumulator (alpha, bias, bf16), arrive on the leader's
+//               accumulator-free barrier, then TMA-store the rows.
+// Per SM and stage this moves 38 KB into shared memory instead of 54 KB, so
+// five stages fit where the one-CTA kernel holds four.  Every mbarrier wait is
 // bounded; all threads meet at one final cluster barrier before the TMEM is
 // released.
 #include <cuda_bf16.h>
@@ -39,70 +47,71 @@ constexpr uint32_t kABytes = kRowsCta * kBKBytes;     // 16 KB: this CTA's A row
 constexpr uint32_t kBBytes = kRowsCta * kBKBytes;     // 16 KB: this CTA's half of B
 constexpr uint32_t kSfaBytes = 4 * 512;               // this CTA's A band, 4 K-steps
 constexpr uint32_t kSfbBytes = 2 * 4 * 512;           // both B bands of the tile
+constexpr uint32_t kOutChunkBytes = 32 * 16 * 2;      // output staging: 32 rows x 16 columns bf16
 constexpr uint32_t kOffA = 0;
 constexpr uint32_t kOffB = kOffA + kStages * kABytes;
 constexpr uint32_t kOffSfa = kOffB + kStages * kBBytes;
 constexpr uint32_t kOffSfb = kOffSfa + kStages * kSfaBytes;
-constexpr uint32_t kOffBias = kOffSfb + kStages * kSfbBytes;   // per epilogue warp: one tile of bias
-constexpr uint32_t kOffBar = kOffBias + 4 * kTileN * 2;
-constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
+constexpr uint32_t kOffBias = kOffSfb + kStages * kSfbBytes;  // two tiles of bias (bf16)
+constexpr uint32_t kOffOut = kOffBias + 2 * kTileN * 2;       // per epilogue warp: two staging chunks
+constexpr uint32_t kOffBar = kOffOut + 8 * 2 * kOutChunkBytes;
+constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;         // barriers + alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemSf = 256;
 constexpr uint32_t kSfColsPerStage = 48;
 constexpr uint64_t kWaitNs = 2000000000ull;
-constexpr int kThreads = 256;
-constexpr int kEpiWarp0 = 4;
-constexpr int kEpiWarps = 4;
-constexpr int kCopiers = 2;                     // lane 0 of warps 2 and 3 (leader): two K-steps each
-
-// Copier index of a thread (-1 if it does not copy scales).  The copiers sit
-// in different warps: a warp issues a tcgen05 instruction for one lane only.
-__device__ __forceinline__ int copier_of(int warp, int lane)
-{
-    return lane == 0 ? (warp == 2 ? 0 : warp == 3 ? 1 : -1) : -1;
-}
+constexpr int kThreads = 512;
+constexpr int kSfWarp0 = 4;
+constexpr int kEpiWarp0 = 8;
+constexpr int kEpiWarps = 8;
+constexpr int kEpiCols = kTileN / 2;
 constexpr uint16_t kBothCtas = 0x3;
+constexpr uint32_t kRegsCtl = 56, kRegsSf = 96, kRegsEpi = 176;
 
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kOffOut % 128 == 0, "TMA store sources are 128-byte aligned");
 static_assert(kTmemSf + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
+static_assert(128 * (kRegsCtl + kRegsSf + 2 * kRegsEpi) <= kThreads * 128, "register reallocation budget");
 
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_nvf4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                          const GemmParams p)
+                          const __grid_constant__ CUtensorMap tmOut, const GemmParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kOffBar);   // this CTA's copies landed
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kOffBar);   // this CTA's stage landed
     uint64_t *empty = full + kStages;                                 // the pair's MMAs released the stage
-    uint64_t *peer_full = empty + kStages;                            // (leader) the peer's copies landed
-    uint64_t *sf_ready = peer_full + kStages;                         // (leader) scales are in both TMEMs
+    uint64_t *sf_ready = empty + kStages;                             // (leader) both CTAs' scales staged
     uint64_t *tmem_full = sf_ready + kStages;                         // accumulator complete
     uint64_t *tmem_empty = tmem_full + 1;                             // (leader) both CTAs drained it
     uint64_t *mma_done = tmem_empty + 1;
-    uint64_t *cp_done = mma_done + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(cp_done + 1);
+    uint64_t *bias_full = mma_done + 1;                               // [2]
+    uint64_t *bias_empty = bias_full + 2;                             // [2]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bias_empty + 2);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
-    const bool leader = rank == 0;
+    const bool is_leader = rank == 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
-            mbar_init(&peer_full[s], 1);
-            mbar_init(&sf_ready[s], kCopiers);
+            mbar_init(&sf_ready[s], 2 * 4);
         }
         mbar_init(tmem_full, 1);
         mbar_init(tmem_empty, 2 * kEpiWarps);
         mbar_init(mma_done, 1);
-        mbar_init(cp_done, kCopiers);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bias_full[b], 1);
+            mbar_init(&bias_empty[b], kEpiWarps);
+        }
         fence_mbarrier_init();
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
     }
-    if (warp == 2) {
+    if (warp == 1) {
         tmem_alloc_pair(tmem_slot, kTmemCols);
         tmem_relinquish_pair();
     }
@@ -118,174 +127,240 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int num_ks = (p.num_k64 + 3) / 4;
     const int a_bands = (p.m + 127) / 128;
 
-    if (warp == 0 && lane == 0) {
-        // ------------------------------------------------------ producer --
-        const uint64_t pol = l2_policy_evict_last();
-        int stage = 0;
-        uint32_t phase = 0;
-        uint32_t issued_mask = 0, issued_phase = 0;
-        bool ok = true;
-        for (int tile = pair_id; tile < num_tiles && ok; tile += num_pairs) {
-            const Tile t = tile_coord(tile, p.num_m_blk, p.num_n_blk);
-            const int band_a = t.mb * 2 + (int)rank;
-            const bool a_here = band_a < a_bands;
-            const int n_rows = min(kTileN, p.n_out - t.nb * kTileN);
-            const int halves = n_rows > 128 ? 2 : 1;
-            for (int ks = 0; ks < num_ks; ++ks) {
-                if (!mbar_wait_cluster(&empty[stage], phase ^ 1, p.err_flag, kErrTimeout, kWaitNs)) { ok = false; break; }
-                const int kcount = min(4, p.num_k64 - ks * 4);
-                const uint32_t sf_bytes = (uint32_t)kcount * 512;
-                mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes + sf_bytes * ((a_here ? 1 : 0) + halves));
-                tma_load_2d(smem + kOffA + stage * kABytes, &tmA, &full[stage], ks * kBKBytes, band_a * kRowsCta, pol);
-                tma_load_2d(smem + kOffB + stage * kBBytes, &tmB, &full[stage], ks * kBKBytes,
-                            t.nb * kTileN + (int)rank * kRowsCta, pol);
-                if (a_here)
-                    bulk_load(smem + kOffSfa + stage * kSfaBytes, p.sfa + band_a * p.sfa_band_bytes + (int64_t)ks * 2048,
-                              sf_bytes, &full[stage], pol);
-                for (int h = 0; h < halves; ++h)
-                    bulk_load(smem + kOffSfb + stage * kSfbBytes + h * 2048,
-                              p.sfb + (t.nb * 2 + h) * p.sfb_band_bytes + (int64_t)ks * 2048, sf_bytes, &full[stage],
-                              pol);
-                issued_mask |= 1u << stage;
-                issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-                if (++stage == kStages) { stage = 0; phase ^= 1; }
-            }
-        }
-        for (int s = 0; s < kStages; ++s)
-            if (issued_mask & (1u << s))
-                mbar_wait(&full[s], (issued_phase >> s) & 1u, p.err_flag, kErrTimeout, kWaitNs);
-    } else if (copier_of(warp, lane) >= 0 && (leader || warp == 3)) {
-        // -------------------- scale copiers (leader) / relay thread (peer) --
-        // In the leader, copier c moves K-steps 2c and 2c+1 of each stage's
-        // scale tiles into both CTAs' TMEM (tcgen05.cp.cta_group::2) once both
-        // CTAs' copies have landed, and commits to sf_ready[stage] (two arrivals).  In the
-        // peer, one thread relays "this CTA's stage landed" to the leader.
-        const int cidx = copier_of(warp, lane);
-        int stage = 0;
-        uint32_t phase = 0;
-        const uint32_t sfa_base = smem_u32(smem + kOffSfa);
-        const uint32_t sfb_base = smem_u32(smem + kOffSfb);
-        const uint32_t leader_peer_full = mapa_shared(peer_full, 0);
-        bool ok = true;
-        for (int tile = pair_id; tile < num_tiles && ok; tile += num_pairs) {
-            const Tile t = tile_coord(tile, p.num_m_blk, p.num_n_blk);
-            const int n_rows = min(kTileN, p.n_out - t.nb * kTileN);
-            const int halves = n_rows > 128 ? 2 : 1;
-            for (int ks = 0; ks < num_ks; ++ks) {
-                if (!mbar_wait(&full[stage], phase, p.err_flag, kErrTimeout, kWaitNs)) { ok = false; break; }
-                if (!leader) {
-                    mbar_arrive_cluster(leader_peer_full + stage * (uint32_t)sizeof(uint64_t));
-                } else {
-                    if (!mbar_wait_cluster(&peer_full[stage], phase, p.err_flag, kErrTimeout, kWaitNs)) { ok = false; break; }
-                    tc_fence_after_sync();
-                    const int kcount = min(4, p.num_k64 - ks * 4);
-                    const uint32_t sf_col = tmem + kTmemSf + stage * kSfColsPerStage;
-                    for (int kk = 2 * cidx; kk < 2 * cidx + 2 && kk < kcount; ++kk) {
-                        tc_cp_pair_32x128b_warpx4(sf_col + kk * 4, smem_desc_sf(sfa_base + stage * kSfaBytes + kk * 512));
-                        for (int h = 0; h < halves; ++h)
-                            tc_cp_pair_32x128b_warpx4(sf_col + 16 + kk * 8 + h * 4,
-                                                      smem_desc_sf(sfb_base + stage * kSfbBytes + h * 2048 + kk * 512));
-                    }
-                    tc_commit_pair(&sf_ready[stage]);
-                }
-                if (++stage == kStages) { stage = 0; phase ^= 1; }
-            }
-        }
-        if (leader) {
-            tc_commit_pair(cp_done);
-            mbar_wait(cp_done, 0, p.err_flag, kErrTimeout, kWaitNs);
-        }
-    } else if (warp == 1 && lane == 0 && leader) {
-        // ---------------------------------------------------- MMA (leader) --
-        int stage = 0;
-        uint32_t phase = 0, acc_phase = 0;
-        const uint32_t a_base = smem_u32(smem + kOffA);
-        const uint32_t b_base = smem_u32(smem + kOffB);
-        const uint32_t idesc = idesc_nvf4(kTileM, kTileN);
-        bool ok = true;
-        for (int tile = pair_id; tile < num_tiles && ok; tile += num_pairs) {
-            if (!mbar_wait_cluster(tmem_empty, acc_phase ^ 1, p.err_flag, kErrTimeout, kWaitNs)) break;
-            tc_fence_after_sync();
-            for (int ks = 0; ks < num_ks; ++ks) {
-                if (!mbar_wait(&sf_ready[stage], phase, p.err_flag, kErrTimeout, kWaitNs)) { ok = false; break; }
-                tc_fence_after_sync();
-                const int kcount = min(4, p.num_k64 - ks * 4);
-                const uint32_t sf_col = tmem + kTmemSf + stage * kSfColsPerStage;
-                const uint64_t adesc = smem_desc_sw128(a_base + stage * kABytes);
-                const uint64_t bdesc = smem_desc_sw128(b_base + stage * kBBytes);
-                for (int kk = 0; kk < kcount; ++kk)
-                    tc_mma_pair_nvf4(tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc,
-                                     sf_col + kk * 4, sf_col + 16 + kk * 8, (ks | kk) != 0);
-                tc_commit_pair_multicast(&empty[stage], kBothCtas);
-                if (++stage == kStages) { stage = 0; phase ^= 1; }
-            }
-            if (!ok) break;
-            tc_commit_pair_multicast(tmem_full, kBothCtas);
-            acc_phase ^= 1;
-        }
-        tc_commit_pair(mma_done);
-        mbar_wait(mma_done, 0, p.err_flag, kErrTimeout, kWaitNs);
-    } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiWarps) {
+    if (warp >= kEpiWarp0) {
+        setmaxnreg_inc<kRegsEpi>();
         // ------------------------------------------------------ epilogue --
         const int q = warp & 3;
-        uint16_t *s_bias = reinterpret_cast<uint16_t *>(smem + kOffBias) + (warp - kEpiWarp0) * kTileN;
+        const int hcol = ((warp - kEpiWarp0) >> 2) * kEpiCols;
+        const uint32_t acc = tmem + ((uint32_t)(q * 32) << 16) + hcol;
+        const uint32_t out_stage = smem_u32(smem + kOffOut) + (warp - kEpiWarp0) * 2 * kOutChunkBytes;
         const uint32_t leader_tmem_empty = mapa_shared(tmem_empty, 0);
+        const bool use_bias = p.bias != nullptr;
         const float alpha = __ldg(p.alpha);
         uint32_t acc_phase = 0;
-        for (int tile = pair_id; tile < num_tiles; tile += num_pairs) {
+        int it = 0;
+        for (int tile = pair_id; tile < num_tiles; tile += num_pairs, ++it) {
             const Tile t = tile_coord(tile, p.num_m_blk, p.num_n_blk);
-            const int n_rows = min(kTileN, p.n_out - t.nb * kTileN);
-            const int col_base = t.nb * kTileN;
-            if (p.bias != nullptr) {
-                __syncwarp();
-                for (int j = lane; j < kTileN; j += 32)
-                    s_bias[j] = (j < n_rows) ? p.bias[col_base + j] : (uint16_t)0;
-                __syncwarp();
-            }
-            if (!mbar_wait_cluster(tmem_full, acc_phase, p.err_flag, kErrTimeout, kWaitNs)) break;
+            const int n_cols = min(kEpiCols, p.n_out - t.nb * kTileN - hcol);   // may be <= 0
+            const int col_base = t.nb * kTileN + hcol;
+            const uint16_t *s_bias = reinterpret_cast<const uint16_t *>(smem + kOffBias) + (it & 1) * kTileN + hcol;
+            if (use_bias &&
+                !__all_sync(~0u, mbar_wait(&bias_full[it & 1], (it >> 1) & 1, p.err_flag, kErrTimeout, kWaitNs)))
+                break;
+            if (!__all_sync(~0u, mbar_wait(tmem_full, acc_phase, p.err_flag, kErrTimeout, kWaitNs))) break;
             tc_fence_after_sync();
-            uint32_t packed[kTileN / 2];
+            acc_phase ^= 1;
+
+            uint32_t r0[32], r1[32];
+            uint32_t packed[kEpiCols / 2];
+            if (n_cols > 0) tmem_ld_32cols(acc, r0);
 #pragma unroll
-            for (int ch = 0; ch < kTileN / 32; ++ch) {
-                if (ch * 32 < n_rows) {
-                    uint32_t r[32];
-                    tmem_ld_32cols(tmem + ((uint32_t)(q * 32) << 16) + ch * 32, r);
-                    tmem_ld_wait();
+            for (int ch = 0; ch < kEpiCols / 32; ++ch) {
+                uint32_t(&cur)[32] = (ch & 1) ? r1 : r0;
+                uint32_t(&nxt)[32] = (ch & 1) ? r0 : r1;
+                if (ch * 32 < n_cols) {                         // uniform across the warp
+                    tmem_ld_wait_regs(cur);
+                    if (ch + 1 < kEpiCols / 32 && (ch + 1) * 32 < n_cols) tmem_ld_32cols(acc + (ch + 1) * 32, nxt);
 #pragma unroll
                     for (int j = 0; j < 32; j += 2) {
                         float b0 = 0.0f, b1 = 0.0f;
-                        if (p.bias != nullptr) {
+                        if (use_bias) {
                             const uint32_t bw = *reinterpret_cast<const uint32_t *>(s_bias + ch * 32 + j);
                             b0 = __uint_as_float(bw << 16);
                             b1 = __uint_as_float(bw & 0xFFFF0000u);
                         }
-                        const uint32_t lo = bf16_bits_rn(__fmaf_rn(__uint_as_float(r[j]), alpha, b0));
-                        const uint32_t hi = bf16_bits_rn(__fmaf_rn(__uint_as_float(r[j + 1]), alpha, b1));
-                        packed[ch * 16 + j / 2] = lo | (hi << 16);
+                        packed[ch * 16 + j / 2] = bf16x2_rn(__fmaf_rn(__uint_as_float(cur[j]), alpha, b0),
+                                                            __fmaf_rn(__uint_as_float(cur[j + 1]), alpha, b1));
                     }
                 }
             }
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(leader_tmem_empty);
-            acc_phase ^= 1;
+            if (lane == 0) {
+                mbar_arrive_remote(leader_tmem_empty);
+                if (use_bias) mbar_arrive(&bias_empty[it & 1]);
+            }
 
-            const int64_t row = (int64_t)t.mb * kTileM + (int64_t)rank * kRowsCta + q * 32 + lane;
-            if (row < p.m) {
-                uint16_t *orow = p.out + row * p.ldo + col_base;
+            // TMA stores of 16-column chunks through two staging buffers; rows
+            // >= m and columns >= n_out are clipped by the TMA.
+            const int row0 = t.mb * kTileM + (int)rank * kRowsCta + q * 32;
 #pragma unroll
-                for (int v = 0; v < kTileN / 8; ++v) {
-                    if (v * 8 + 8 <= n_rows) {
-                        *reinterpret_cast<uint4 *>(orow + v * 8) =
-                            make_uint4(packed[v * 4], packed[v * 4 + 1], packed[v * 4 + 2], packed[v * 4 + 3]);
-                    } else if (v * 8 < n_rows) {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            if (v * 8 + e < n_rows)
-                                orow[v * 8 + e] = (uint16_t)(packed[v * 4 + e / 2] >> ((e & 1) * 16));
+            for (int c = 0; c < kEpiCols / 16; ++c) {
+                if (c * 16 < n_cols) {                          // uniform across the warp
+                    const uint32_t buf = out_stage + (c & 1) * kOutChunkBytes;
+                    if (lane == 0) bulk_wait_group_read<1>();   // the store that last read `buf` is done with it
+                    __syncwarp();
+                    st_shared_v4(buf + lane * 32, packed[c * 8], packed[c * 8 + 1], packed[c * 8 + 2],
+                                 packed[c * 8 + 3]);
+                    st_shared_v4(buf + lane * 32 + 16, packed[c * 8 + 4], packed[c * 8 + 5], packed[c * 8 + 6],
+                                 packed[c * 8 + 7]);
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmOut, buf, col_base + c * 16, row0);
+                        bulk_commit_group();
                     }
                 }
             }
+        }
+        if (lane == 0) bulk_wait_group<0>();                    // all output written before the CTA exits
+    } else if (warp >= kSfWarp0) {
+        setmaxnreg_dec<kRegsSf>();
+        // ----------------------------------------------- scale staging --
+        // tcgen05.cp 32x128b.warpx4 layout: lane 32q + i of quarter q gets
+        // bytes [16i, 16i + 16) of each 512-byte scale tile.  A stage's TMEM
+        // columns are rewritten only after the stage landed again, i.e. after
+        // the MMAs that read them completed and released it.
+        const int q = warp & 3;
+        const uint32_t sf_tmem = tmem + ((uint32_t)(q * 32) << 16) + kTmemSf;
+        const uint32_t sfa_smem = smem_u32(smem + kOffSfa) + lane * 16;
+        const uint32_t sfb_smem = smem_u32(smem + kOffSfb) + lane * 16;
+        const uint32_t leader_sf_ready = mapa_shared(sf_ready, 0);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int tile = pair_id; tile < num_tiles && ok; tile += num_pairs) {
+            for (int ks = 0; ks < num_ks; ++ks) {
+                ok = __all_sync(~0u, mbar_wait(&full[stage], phase, p.err_flag, kErrTimeout, kWaitNs));
+                if (!ok) break;
+                uint32_t a[16], b[32];
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint4 v = ld_shared_v4(sfa_smem + stage * kSfaBytes + kk * 512);
+                    a[kk * 4 + 0] = v.x; a[kk * 4 + 1] = v.y; a[kk * 4 + 2] = v.z; a[kk * 4 + 3] = v.w;
+                }
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint4 v = ld_shared_v4(sfb_smem + stage * kSfbBytes + h * 2048 + kk * 512);
+                        uint32_t *d = b + kk * 8 + h * 4;
+                        d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
+                    }
+                // (tiles past the valid K-steps, B rows or A rows hold stale
+                // bytes; what they meet in the MMA is never stored)
+                tmem_st_16cols(sf_tmem + stage * kSfColsPerStage, a);
+                tmem_st_32cols(sf_tmem + stage * kSfColsPerStage + 16, b);
+                tmem_st_wait();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(leader_sf_ready + stage * (uint32_t)sizeof(uint64_t));
+                if (++stage == kStages) { stage = 0; phase ^= 1; }
+            }
+        }
+    } else {
+        setmaxnreg_dec<kRegsCtl>();
+        if (warp == 0 && lane == 0) {
+            // ------------------------------------------------------ producer --
+            const uint64_t pol = l2_policy_evict_last();
+            auto issue_w = [&](int stage, const Tile &t, int ks) {
+                const int n_rows = min(kTileN, p.n_out - t.nb * kTileN);
+                const int halves = n_rows > 128 ? 2 : 1;
+                const bool a_here = t.mb * 2 + (int)rank < a_bands;
+                const uint32_t sf_bytes = (uint32_t)min(4, p.num_k64 - ks * 4) * 512;
+                mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes + sf_bytes * ((a_here ? 1 : 0) + halves));
+                tma_load_2d(smem + kOffB + stage * kBBytes, &tmB, &full[stage], ks * kBKBytes,
+                            t.nb * kTileN + (int)rank * kRowsCta, pol);
+                for (int h = 0; h < halves; ++h)
+                    bulk_load(smem + kOffSfb + stage * kSfbBytes + h * 2048,
+                              p.sfb + (t.nb * 2 + h) * p.sfb_band_bytes + (int64_t)ks * 2048, sf_bytes, &full[stage],
+                              pol);
+            };
+            auto issue_a = [&](int stage, const Tile &t, int ks) {
+                const int band_a = t.mb * 2 + (int)rank;
+                const uint32_t sf_bytes = (uint32_t)min(4, p.num_k64 - ks * 4) * 512;
+                tma_load_2d(smem + kOffA + stage * kABytes, &tmA, &full[stage], ks * kBKBytes, band_a * kRowsCta,
+                            pol);
+                if (band_a < a_bands)
+                    bulk_load(smem + kOffSfa + stage * kSfaBytes, p.sfa + band_a * p.sfa_band_bytes + (int64_t)ks * 2048,
+                              sf_bytes, &full[stage], pol);
+            };
+            // Weight side of the first fills before the wait on the preceding
+            // grid (the activation quantizer, when launched as its dependent).
+            int pre = 0;
+            for (int tile = pair_id; tile < num_tiles && pre < kStages; tile += num_pairs) {
+                const Tile t = tile_coord(tile, p.num_m_blk, p.num_n_blk);
+                for (int ks = 0; ks < num_ks && pre < kStages; ++ks) issue_w(pre++, t, ks);
+            }
+            griddep_wait();
+            int stage = 0, fill = 0;
+            uint32_t phase = 0;
+            uint32_t issued_mask = 0, issued_phase = 0;
+            bool ok = true;
+            for (int tile = pair_id; tile < num_tiles && ok; tile += num_pairs) {
+                const Tile t = tile_coord(tile, p.num_m_blk, p.num_n_blk);
+                for (int ks = 0; ks < num_ks; ++ks, ++fill) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1, p.err_flag, kErrTimeout, kWaitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    if (fill >= pre) issue_w(stage, t, ks);
+                    issue_a(stage, t, ks);
+                    issued_mask |= 1u << stage;
+                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == kStages) { stage = 0; phase ^= 1; }
+                }
+            }
+            for (int s = 0; s < kStages; ++s)
+                if (issued_mask & (1u << s))
+                    mbar_wait(&full[s], (issued_phase >> s) & 1u, p.err_flag, kErrTimeout, kWaitNs);
+        } else if (warp == 2 && p.bias != nullptr) {
+            // ---------------------------------------------------- bias loader --
+            uint16_t *s_bias_all = reinterpret_cast<uint16_t *>(smem + kOffBias);
+            int it = 0;
+            for (int tile = pair_id; tile < num_tiles; tile += num_pairs, ++it) {
+                const Tile t = tile_coord(tile, p.num_m_blk, p.num_n_blk);
+                const int n_rows = min(kTileN, p.n_out - t.nb * kTileN);
+                const int b = it & 1;
+                if (!__all_sync(~0u, mbar_wait(&bias_empty[b], ((it >> 1) & 1) ^ 1, p.err_flag, kErrTimeout,
+                                               kWaitNs)))
+                    break;
+                for (int j = lane; j < kTileN; j += 32)
+                    s_bias_all[b * kTileN + j] = (j < n_rows) ? p.bias[t.nb * kTileN + j] : (uint16_t)0;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bias_full[b]);
+            }
+        } else if (warp == 1 && is_leader) {
+            // ---------------------------------------------------- MMA (leader) --
+            // The whole warp runs the loop (warp-uniform values); one elected
+            // lane issues the MMAs and commits for both CTAs.
+            const bool issuer = elect_one();
+            int stage = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            const uint32_t a_base = smem_u32(smem + kOffA);
+            const uint32_t b_base = smem_u32(smem + kOffB);
+            const uint32_t idesc = idesc_nvf4(kTileM, kTileN);
+            bool ok = true;
+            for (int tile = pair_id; tile < num_tiles && ok; tile += num_pairs) {
+                if (!__all_sync(~0u, mbar_wait(tmem_empty, acc_phase ^ 1, p.err_flag, kErrTimeout, kWaitNs)))
+                    break;
+                tc_fence_after_sync();
+                for (int ks = 0; ks < num_ks; ++ks) {
+                    if (!__all_sync(~0u, mbar_wait(&sf_ready[stage], phase, p.err_flag, kErrTimeout, kWaitNs))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const int kcount = min(4, p.num_k64 - ks * 4);
+                    const uint32_t sf_col = tmem + kTmemSf + stage * kSfColsPerStage;
+                    const uint64_t adesc = smem_desc_sw128(a_base + stage * kABytes);
+                    const uint64_t bdesc = smem_desc_sw128(b_base + stage * kBBytes);
+                    if (issuer) {
+                        for (int kk = 0; kk < kcount; ++kk)
+                            tc_mma_pair_nvf4(tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc,
+                                             sf_col + kk * 4, sf_col + 16 + kk * 8, (ks | kk) != 0);
+                        tc_commit_pair_multicast(&empty[stage], kBothCtas);
+                    }
+                    if (++stage == kStages) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                if (issuer) tc_commit_pair_multicast(tmem_full, kBothCtas);
+                __syncwarp();
+                acc_phase ^= 1;
+            }
+            if (issuer) tc_commit_pair(mma_done);
+            __syncwarp();
+            mbar_wait(mma_done, 0, p.err_flag, kErrTimeout, kWaitNs);
         }
     }
 
@@ -293,13 +368,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();                       // reconverge the role lanes before the aligned cluster barrier
     cluster_sync_all();                 // no peer access to this CTA's smem or TMEM after this point
     tc_fence_after_sync();
-    if (warp == 2) tmem_dealloc_pair(tmem, kTmemCols);
+    if (warp == 1) tmem_dealloc_pair(tmem, kTmemCols);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_pair(const GemmParams &p_in, const uint8_t *a, const uint8_t *w, int num_sms, cudaStream_t s,
-                             const char **why)
+                             const char **why, bool dependent)
 {
     static int configured_device = -1;
     static int max_pairs = 0;
@@ -329,30 +404,40 @@ cudaError_t launch_gemm_pair(const GemmParams &p_in, const uint8_t *a, const uin
         max_pairs = clusters;
         configured_device = dev;
     }
+    if (p_in.splits != 1) {
+        *why = "the CTA-pair GEMM does not split K";
+        return cudaErrorInvalidValue;
+    }
     GemmParams p = p_in;
     p.num_m_blk = (p.m + kTileM - 1) / kTileM;
-    CUtensorMap tmA, tmB;
+    CUtensorMap tmA, tmB, tmOut;
     const uint64_t row_bytes = (uint64_t)p.kp / 2;
     if (!make_operand_map(&tmA, a, row_bytes, (uint64_t)p.m, kRowsCta) ||
         !make_operand_map(&tmB, w, row_bytes, (uint64_t)p.n_w, kRowsCta)) {
         *why = "cuTensorMapEncodeTiled failed for an FP4 operand";
         return cudaErrorInvalidValue;
     }
+    if (!make_output_map(&tmOut, p.out, (uint64_t)p.n_out, (uint64_t)p.m, (uint64_t)p.ldo)) {
+        *why = "cuTensorMapEncodeTiled failed for the output";
+        return cudaErrorInvalidValue;
+    }
     const int tiles = p.num_m_blk * p.num_n_blk;
     const int pairs = tiles < max_pairs ? tiles : max_pairs;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = 2;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
+    cudaLaunchAttribute attrs[2];
+    attrs[0].id = cudaLaunchAttributeClusterDimension;
+    attrs[0].val.clusterDim.x = 2;
+    attrs[0].val.clusterDim.y = 1;
+    attrs[0].val.clusterDim.z = 1;
+    attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(2 * pairs, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = s;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_nvf4_pair_kernel, tmA, tmB, p);
+    cfg.attrs = attrs;
+    cfg.numAttrs = dependent ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, gemm_nvf4_pair_kernel, tmA, tmB, tmOut, p);
 }
 
 }  // namespace nvfp4
