@@ -129,7 +129,7 @@ def load_peaks():
 
 def gemm_source_hash() -> str:
     h = hashlib.sha256()
-    for name in ("gemm.cu", "ptx.cuh", "common.cuh"):
+    for name in ("gemm.cu", "gemm_common.cuh", "ptx.cuh", "common.cuh"):
         with open(os.path.join(ROOT, "nvfp4_quantized_linear_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
