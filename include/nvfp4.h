@@ -109,7 +109,7 @@ size_t nvfp4_scale_bytes(int64_t rows, int64_t k);
 
 /* Workspace nvfp4_linear wants for an m x k activation against n_w weight
  * rows: the quantized activation and its scales (each 256-B aligned inside)
- * and, for m <= 128, room for split-K partial sums (160 * 256 fp32 per row).
+ * and, for m <= 128, room for split-K partial sums (640 * 256 fp32 per row).
  * nvfp4_linear accepts any workspace that holds the first two; given less than
  * this size, a small-m call runs without split-K. */
 size_t nvfp4_linear_workspace_bytes(int64_t m, int64_t k, int64_t n_w);

@@ -240,22 +240,40 @@ nvfp4::GemmParams gemm_params(const uint8_t *a_sf, int64_t m, const uint8_t *w_s
     return g;
 }
 
-// Split-K plan for small m (a single 128-row band): when the output has too
-// few 128 x 256 tiles to occupy every SM, cut K into ranges so that tiles x
-// splits is close to the SM count.  Returns the number of splits (1: none) and
-// sets the stages per split such that no range is empty.
+// Split-K plan for small m (a single 128-row band), where the GEMM streams the
+// weight and one CTA per 128 x 256 output tile leaves SMs idle.  K is cut
+// into `splits` ranges of whole 256-element stages, choosing the count with
+// the least estimated cost in stage units: the stage-waves
+// ceil(tiles * splits / SMs) * ceil(stages / splits), plus, when split, the
+// fp32 partials each work item writes (m KB, stored row by row) and the reduce
+// reads back, priced at 4 * m KB-equivalents per item and wave against about
+// 36 KB of weight and scales per stage (measured: splitting pays for m = 1 on
+// every layer shape, but at m = 128 only when K is long).  Fewest splits on
+// ties; at most kMaxSplits and four waves of work items; every range
+// non-empty.  Returns the number of splits (1: none) and the stages per split.
 int split_k_plan(const nvfp4::GemmParams &g, int num_sms, int *stages_per_split)
 {
     const int num_ks = (g.num_k64 + 3) / 4;
     *stages_per_split = num_ks;
-    if (g.m > 128) return 1;
-    const int tiles = g.num_n_blk;
-    if (tiles * 2 > num_sms) return 1;
-    int s = num_sms / tiles;
-    if (s > num_ks) s = num_ks;
-    if (s > nvfp4::kMaxSplits) s = nvfp4::kMaxSplits;
-    if (s < 2) return 1;
-    const int sps = (num_ks + s - 1) / s;
+    if (g.m > 128 || num_sms <= 0) return 1;
+    const int64_t tiles = g.num_n_blk;
+    // costs in KB of traffic per SM (one stage ~ 36 KB)
+    int best_s = 1;
+    int64_t best_cost = ((tiles + num_sms - 1) / num_sms) * num_ks * 36;
+    for (int s = 2; s <= nvfp4::kMaxSplits && s <= num_ks; ++s) {
+        const int sps = (num_ks + s - 1) / s;
+        const int used = (num_ks + sps - 1) / sps;           // splits actually non-empty
+        const int64_t items = tiles * used;
+        if (items > 4 * (int64_t)num_sms) break;
+        const int64_t waves = (items + num_sms - 1) / num_sms;
+        const int64_t cost = waves * (sps * 36 + 4 * (int64_t)g.m);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best_s = s;
+        }
+    }
+    if (best_s == 1) return 1;
+    const int sps = (num_ks + best_s - 1) / best_s;
     *stages_per_split = sps;
     return (num_ks + sps - 1) / sps;
 }
@@ -266,9 +284,10 @@ size_t split_k_bytes(const nvfp4::GemmParams &g, int splits)
     return (size_t)splits * (size_t)g.m * (size_t)g.num_n_blk * 256 * sizeof(float);
 }
 
-// Upper bound of split_k_bytes for any device of up to 160 SMs: splits x tiles
-// never exceeds the SM count, so the partials never exceed 160 x 256 floats per row.
-constexpr size_t kSplitBytesPerRow = 160 * 256 * sizeof(float);
+// Room nvfp4_linear_workspace_bytes reserves for split-K partials, per row of
+// m: four waves of work items on a device of up to 160 SMs, 256 fp32 each.
+// A plan whose partials do not fit runs unsplit.
+constexpr size_t kSplitBytesPerRow = 4 * 160 * 256 * sizeof(float);
 
 // Launches the GEMM; with `partials` (scratch of partial_bytes bytes) and a
 // small m it may split K and finish with the reduce kernel.  after_quant: the

@@ -168,6 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t out_stage = smem_u32(smem + kOffOut) + (warp - kEpiWarp0) * kOutChunkBytes;
         const bool use_bias = p.splits == 1 && p.bias != nullptr;
         const float alpha = __ldg(p.alpha);
+        const uint64_t out_policy = l2_policy_evict_first();   // the output is written once
         uint32_t acc_phase = 0;
         int it = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
@@ -258,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fence_proxy_async_shared();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&tmOut, out_stage, col_base + c * 16, row0);
+                        tma_store_2d(&tmOut, out_stage, col_base + c * 16, row0, out_policy);
                         bulk_commit_group();
                     }
                 }
@@ -317,7 +318,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp == 0 && lane == 0) {
             // ------------------------------------------------------ producer --
             const uint64_t pol_a = l2_policy_evict_last();
-            const uint64_t pol_b = l2_policy_evict_last();
+            // weights are re-read by every 128-row band; with one band they stream once
+            const uint64_t pol_b = p.num_m_blk == 1 ? l2_policy_evict_first() : l2_policy_evict_last();
             // Weight side (B tile and its scale tiles) of one stage fill; arms
             // the stage's barrier with the bytes of the whole fill.
             auto issue_w = [&](int stage, const Work &wk, int ks) {

@@ -137,6 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t leader_tmem_empty = mapa_shared(tmem_empty, 0);
         const bool use_bias = p.bias != nullptr;
         const float alpha = __ldg(p.alpha);
+        const uint64_t out_policy = l2_policy_evict_first();   // the output is written once
         uint32_t acc_phase = 0;
         int it = 0;
         for (int tile = pair_id; tile < num_tiles; tile += num_pairs, ++it) {
@@ -197,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fence_proxy_async_shared();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&tmOut, buf, col_base + c * 16, row0);
+                        tma_store_2d(&tmOut, buf, col_base + c * 16, row0, out_policy);
                         bulk_commit_group();
                     }
                 }

@@ -104,10 +104,11 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
 
 // 2-D tiled TMA store from this CTA's shared memory (bulk-group completion);
 // elements outside the tensor map's extent are not written.
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src_smem, int32_t x, int32_t y)
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src_smem, int32_t x, int32_t y,
+                                             uint64_t l2_policy)
 {
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map),
-                 "r"(src_smem), "r"(x), "r"(y)
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;"
+                 ::"l"(map), "r"(src_smem), "r"(x), "r"(y), "l"(l2_policy)
                  : "memory");
 }
 
@@ -559,6 +560,16 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void *p)
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                  : "l"(p));
+    return r;
+}
+
+// The same with an L2 eviction policy (e.g. evict-first for data read once).
+__device__ __forceinline__ uint4 ld_stream_v4(const void *p, uint64_t l2_policy)
+{
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p), "l"(l2_policy));
     return r;
 }
 

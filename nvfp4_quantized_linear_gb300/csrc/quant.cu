@@ -15,6 +15,7 @@
 
 #include "common.cuh"
 #include "ptx.cuh"
+#include "scale_math.cuh"
 
 namespace nvfp4 {
 namespace {
@@ -24,21 +25,42 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// Scale code and element multiplier of a block with absolute maximum `amax`.
-__device__ __forceinline__ uint32_t block_scale(float amax, float gs, float &inv)
+// Scale code and element multiplier of a block with absolute maximum `amax`:
+//   s = (amax * gs) / 6;  sf = e4m3(s);  inv = sf ? gs / e4m3(sf) : 0.
+// The division by 6 is div6_rn (scale_math.cuh), which gives the same code sf
+// as the IEEE quotient for every input.  gs / e4m3(code) comes from a table of
+// the 128 non-negative codes (s >= 0, and satfinite never yields the NaN code)
+// that each block fills once with the IEEE division (fill_inv_table).
+__device__ __forceinline__ uint32_t block_scale_tab(float amax, float gs, const float *inv_tab, float &inv)
 {
-    const float s = __fdiv_rn(__fmul_rn(amax, gs), 6.0f);
-    const uint32_t sf = cvt_e4m3x2(0.0f, s) & 0xFFu;
-    const float d = e4m3_to_f32(sf);
-    inv = (d == 0.0f) ? 0.0f : __fdiv_rn(gs, d);
+    const float s = div6_rn(__fmul_rn(amax, gs));
+    const uint32_t sf = cvt_e4m3x2(0.0f, s) & 0x7Fu;
+    inv = inv_tab[sf];
     return sf;
 }
 
+__device__ __forceinline__ void fill_inv_table(float *inv_tab, float gs)
+{
+    for (int c = threadIdx.x; c < 128; c += blockDim.x) {
+        const float d = e4m3_to_f32((uint32_t)c);
+        inv_tab[c] = (d == 0.0f) ? 0.0f : __fdiv_rn(gs, d);
+    }
+}
+
+// q_i = e2m1(v_i * inv), the products two at a time (mul.rn.f32x2: each lane
+// of the pair rounds like a scalar fp32 multiply).
 __device__ __forceinline__ uint32_t quant8(const float (&v)[8], float inv)
 {
     float q[8];
+    uint64_t iv;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(iv) : "f"(inv));
 #pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] = __fmul_rn(v[i], inv);
+    for (int i = 0; i < 8; i += 2) {
+        uint64_t a, d;
+        asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(v[i]), "f"(v[i + 1]));
+        asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(iv));
+        asm("mov.b64 {%0, %1}, %2;" : "=f"(q[i]), "=f"(q[i + 1]) : "l"(d));
+    }
     return cvt_e2m1x8(q);
 }
 
@@ -93,7 +115,10 @@ __global__ void __launch_bounds__(256) quant_kernel(const QuantParams p)
     // A programmatic dependent (the GEMM of the linear layer) may start its
     // prologue now; it waits for this grid before touching its data.
     if (threadIdx.x == 0) griddep_launch_dependents();
+    __shared__ float inv_tab[128];
     const float gs = __ldg(p.gs);
+    fill_inv_table(inv_tab, gs);
+    __syncthreads();
     const int segs = (p.kp + 511) >> 9;
     const int tasks = p.mp * segs;                    // < 2^31: checked on the host
     const int64_t out_ld = p.kp >> 1;
@@ -123,7 +148,7 @@ __global__ void __launch_bounds__(256) quant_kernel(const QuantParams p)
 #pragma unroll
             for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(v0[i]), fabsf(v1[i])));
             float inv;
-            const uint32_t sf = block_scale(amax, gs, inv);
+            const uint32_t sf = block_scale_tab(amax, gs, inv_tab, inv);
             if (r < p.m && k0 < p.kp) {
                 uint2 pk;
                 pk.x = quant8(v0, inv);
@@ -158,8 +183,10 @@ __global__ void __launch_bounds__(256) quant_transform_kernel(const QuantParams 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) griddep_launch_dependents();    // as in quant_kernel
 
+    __shared__ float inv_tab[128];
     for (int i = tid; i < bs * bs; i += 256) sT[i] = __uint_as_float((uint32_t)p.t[i] << 16);
     const float gs = __ldg(p.gs);
+    fill_inv_table(inv_tab, gs);                           // visible after the first tile's barrier
     const int segs = (p.kp + 255) >> 8;
     const int64_t tiles = (int64_t)(p.mp / 32) * segs;
     const int64_t out_ld = p.kp >> 1;
@@ -227,7 +254,7 @@ __global__ void __launch_bounds__(256) quant_transform_kernel(const QuantParams 
                 amax = fmaxf(amax, fmaxf(fabsf(y0[j]), fabsf(y1[j])));
             }
             float inv;
-            const uint32_t sf = block_scale(amax, gs, inv);
+            const uint32_t sf = block_scale_tab(amax, gs, inv_tab, inv);
             if (r < p.m) {
                 uint2 pk;
                 pk.x = quant8(y0, inv);

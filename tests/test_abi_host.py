@@ -56,9 +56,9 @@ def test_size_queries(lib):
     ws = nv.nvfp4_linear_workspace_bytes(100, 1000, 512)
     assert ws >= nv.nvfp4_packed_bytes(100, 1000) + nv.nvfp4_scale_bytes(100, 1000)
     assert nv.nvfp4_linear_workspace_bytes(0, 1000, 512) == 0
-    # m <= 128 adds room for split-K partials (160 x 256 fp32 per row); larger m does not
+    # m <= 128 adds room for split-K partials (640 x 256 fp32 per row); larger m does not
     base = lambda m, k: (nv.nvfp4_packed_bytes(m, k) + 255) // 256 * 256 + (nv.nvfp4_scale_bytes(m, k) + 255) // 256 * 256
-    assert ws == base(100, 1000) + 160 * 256 * 4 * 100
+    assert ws == base(100, 1000) + 640 * 256 * 4 * 100
     assert nv.nvfp4_linear_workspace_bytes(129, 1000, 512) == base(129, 1000)
 
 

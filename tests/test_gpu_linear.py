@@ -110,10 +110,10 @@ def test_linear_rejects_small_workspace():
 
 SPLIT_K = [syn.Problem("splitk", f"m{m}-n{n}-k{k}", m, k, n, seed=1300 + i, bias=bias, n_out=n_out)
            for i, (m, k, n, n_out, bias) in enumerate([
-               (1, 4096, 256, None, False),      # one output tile: 16 splits of 4 stages
+               (1, 4096, 256, None, False),      # one output tile: 16 splits of one stage
                (5, 4104, 1024, 1000, True),      # ragged K (65 k-steps), sliced output, bias
                (64, 14336, 4096, None, True),    # Llama down_proj width at decode size
-               (128, 2048, 512, 500, False),     # full band, 2 tiles
+               (128, 14336, 512, 500, False),    # full band, 2 tiles, long K: 14 splits of 4 stages
                (33, 64, 256, None, True),        # a single K stage: no split
            ])]
 
