@@ -131,7 +131,7 @@ def load_peaks():
 
 def gemm_source_hash() -> str:
     h = hashlib.sha256()
-    for name in ("gemm.cu", "gemm_common.cuh", "ptx.cuh", "common.cuh"):
+    for name in ("gemm.cu", "gemm_pair.cu", "gemm_common.cuh", "ptx.cuh", "common.cuh"):
         with open(os.path.join(ROOT, "nvfp4_quantized_linear_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -382,7 +382,7 @@ def run_ours(args, rank, world, local_rank):
                    "m": args.m, "layers": [[l["p"].name, l["p"].k, l["p"].n] for l in layers],
                    "l2": "inputs larger than L2 (0.4 GB of activations per step)", "bias": False,
                    "transform": None},
-        "roofline": {"bound": "tensor", "kernel": f"gemm_nvf4_kernel ({layers[top]['p'].name} launch)",
+        "roofline": {"bound": "tensor", "kernel": f"gemm_nvf4_pair_kernel ({layers[top]['p'].name} launch)",
                      "achieved": round(top_tflops, 2), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
                      "frac": round(top_tflops / fp4_peak, 4),
                      "traffic": (round(traffic) if traffic else None),

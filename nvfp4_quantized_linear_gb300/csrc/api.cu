@@ -16,12 +16,14 @@ namespace {
 
 thread_local std::string g_last_error;
 
-// GEMMs run on the one-CTA kernel.  NVFP4_GEMM_PAIR=1 in the environment (read
-// once, when the library loads) sends GEMMs with m > 128 to the CTA-pair kernel
-// instead, which computes the same result.
+// GEMMs with m > 128 run on the CTA-pair kernel (256 x 256 tiles, half of B
+// per SM), smaller ones on the one-CTA kernel (which can split K).  Both compute
+// the same result; NVFP4_GEMM_ONE_CTA=1 in the environment (read once, when the
+// library loads) keeps every GEMM on the one-CTA kernel, so that its m > 128
+// path stays testable.
 const bool g_use_pair_kernel = [] {
-    const char *v = getenv("NVFP4_GEMM_PAIR");
-    return v != nullptr && v[0] == '1';
+    const char *v = getenv("NVFP4_GEMM_ONE_CTA");
+    return !(v != nullptr && v[0] == '1');
 }();
 
 nvfp4_status fail(nvfp4_status st, const char *fmt, ...)

@@ -8,11 +8,12 @@
 // A, B packed E2M1 (K-major) with one UE4M3 scale per 16 K-elements.
 //
 // Design (one CTA per SM, persistent over output tiles of 128 x 256; 16 warps):
-//   warp 0      TMA producer: A tile 128 x 256 FP4 (16 KB), B tile 256 x 256 FP4
-//               (32 KB), both 128-byte swizzled, plus the matching 512-byte
-//               scale tiles by bulk copy, into a 4-stage shared-memory ring.
-//               The weight side of the first fills goes out before the wait
-//               on the preceding grid (programmatic dependent launch);
+//   warps 0, 3  TMA producers (lane 0 of each): warp 0 the A tile 128 x 256
+//               FP4 (16 KB) and its scale tile, warp 3 the B tile 256 x 256 FP4
+//               (32 KB) and its two scale tiles, 128-byte swizzled, into a
+//               4-stage shared-memory ring.  Only warp 0 waits for the
+//               preceding grid (programmatic dependent launch), so the weights
+//               stream while the activation quantizer finishes;
 //   warp 1      allocates / frees the 512 TMEM columns; lane 0 issues the
 //               MMAs: 4 x tcgen05.mma (M=128, N=256, K=64, kind::mxf4nvf4,
 //               scale_vec::4X) per stage into a 128 x 256 fp32 TMEM tile;
@@ -123,7 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], 2);             // the activation and the weight producer
             mbar_init(&empty[s], 1);
             mbar_init(&sf_ready[s], 4);
         }
@@ -315,51 +316,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         setmaxnreg_dec<kRegsCtl>();
-        if (warp == 0 && lane == 0) {
-            // ------------------------------------------------------ producer --
-            const uint64_t pol_a = l2_policy_evict_last();
+        if ((warp == 0 || warp == 3) && lane == 0) {
+            // ----------------------------------------------------- producers --
+            // Two threads fill the ring, each with its half of every stage:
+            // warp 0 the activation side (A tile + its scale tile), warp 3 the
+            // weight side (B tile + the scale tiles of its two bands); each
+            // arms the stage's `full` barrier (two arrivals) with its bytes.
+            // One thread issuing all five copies of a stage took ~630 clocks,
+            // longer than the stage's MMAs.  Only the activation side waits
+            // for the preceding grid (the activation quantizer, when launched
+            // as its programmatic dependent): the weights are not written by
+            // it, so they stream while the quantizer finishes.
+            const bool act_side = warp == 0;
             // weights are re-read by every 128-row band; with one band they stream once
-            const uint64_t pol_b = p.num_m_blk == 1 ? l2_policy_evict_first() : l2_policy_evict_last();
-            // Weight side (B tile and its scale tiles) of one stage fill; arms
-            // the stage's barrier with the bytes of the whole fill.
-            auto issue_w = [&](int stage, const Work &wk, int ks) {
-                const Tile t = wk.t;
-                const int halves = min(kBN, p.n_out - t.nb * kBN) > 128 ? 2 : 1;
-                const uint32_t sf_bytes = (uint32_t)min(4, p.num_k64 - ks * 4) * 512;
-                mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes + sf_bytes * (1 + halves));
-                tma_load_2d(smem + kOffB + stage * kBBytes, &tmB, &full[stage], ks * kBKBytes, t.nb * kBN, pol_b);
-                for (int h = 0; h < halves; ++h)        // halves == 2 implies band t.nb*2+1 exists
-                    bulk_load(smem + kOffSfb + stage * kSfbBytes + h * 2048,
-                              p.sfb + (t.nb * 2 + h) * p.sfb_band_bytes + (int64_t)ks * 2048, sf_bytes, &full[stage],
-                              pol_b);
-            };
-            // Activation side (A tile and its scale tile) of the same fill.
-            auto issue_a = [&](int stage, const Work &wk, int ks) {
-                const uint32_t sf_bytes = (uint32_t)min(4, p.num_k64 - ks * 4) * 512;
-                tma_load_2d(smem + kOffA + stage * kABytes, &tmA, &full[stage], ks * kBKBytes, wk.t.mb * kBM, pol_a);
-                bulk_load(smem + kOffSfa + stage * kSfaBytes, p.sfa + wk.t.mb * p.sfa_band_bytes + (int64_t)ks * 2048,
-                          sf_bytes, &full[stage], pol_a);
-            };
-            // The first kStages fills start with their weight side, before the
-            // wait for the preceding grid: launched as the dependent of the
-            // activation quantizer, the GEMM streams weights (which that grid
-            // does not write) while the quantizer is still running.
-            int pre = 0;
-            for (int tile = blockIdx.x; tile < num_tiles && pre < kStages; tile += gridDim.x) {
-                const Work wk = work_of(tile, p, num_ks);
-                for (int ks = wk.ks0; ks < wk.ks1 && pre < kStages; ++ks) issue_w(pre++, wk, ks);
-            }
-            griddep_wait();
-            int stage = 0, fill = 0;
+            const uint64_t pol = act_side || p.num_m_blk > 1 ? l2_policy_evict_last() : l2_policy_evict_first();
+            if (act_side) griddep_wait();
+            int stage = 0;
             uint32_t phase = 0;
             uint32_t issued_mask = 0, issued_phase = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
                 const Work wk = work_of(tile, p, num_ks);
-                for (int ks = wk.ks0; ks < wk.ks1; ++ks, ++fill) {
+                const Tile t = wk.t;
+                const int halves = min(kBN, p.n_out - t.nb * kBN) > 128 ? 2 : 1;
+                for (int ks = wk.ks0; ks < wk.ks1; ++ks) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, p.err_flag, kErrTimeout, kWaitNs)) { ok = false; break; }
-                    if (fill >= pre) issue_w(stage, wk, ks);
-                    issue_a(stage, wk, ks);
+                    const uint32_t sf_bytes = (uint32_t)min(4, p.num_k64 - ks * 4) * 512;
+                    if (act_side) {
+                        mbar_arrive_expect_tx(&full[stage], kABytes + sf_bytes);
+                        tma_load_2d(smem + kOffA + stage * kABytes, &tmA, &full[stage], ks * kBKBytes, t.mb * kBM, pol);
+                        bulk_load(smem + kOffSfa + stage * kSfaBytes,
+                                  p.sfa + t.mb * p.sfa_band_bytes + (int64_t)ks * 2048, sf_bytes, &full[stage], pol);
+                    } else {
+                        mbar_arrive_expect_tx(&full[stage], kBBytes + sf_bytes * halves);
+                        tma_load_2d(smem + kOffB + stage * kBBytes, &tmB, &full[stage], ks * kBKBytes, t.nb * kBN, pol);
+                        for (int h = 0; h < halves; ++h)    // halves == 2 implies band t.nb*2+1 exists
+                            bulk_load(smem + kOffSfb + stage * kSfbBytes + h * 2048,
+                                      p.sfb + (t.nb * 2 + h) * p.sfb_band_bytes + (int64_t)ks * 2048, sf_bytes,
+                                      &full[stage], pol);
+                    }
                     issued_mask |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == kStages) { stage = 0; phase ^= 1; }
@@ -367,8 +362,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             (void)n_bands_w;
             // Every copy this thread issued has landed before the CTA may exit.
-            // (The pre-issued fills pass the loop above before any wait that can
-            // time out: their empty barriers are fresh.)
             for (int s = 0; s < kStages; ++s)
                 if (issued_mask & (1u << s))
                     mbar_wait(&full[s], (issued_phase >> s) & 1u, p.err_flag, kErrTimeout, kWaitNs);

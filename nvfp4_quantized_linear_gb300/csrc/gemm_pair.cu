@@ -4,11 +4,11 @@
 // section 关键源码片段: _scaled_mm, * alpha, slice, + bias), with each output
 // tile of 256 x 256 computed by a cluster of two CTAs on two SMs.  Per CTA
 // r (r = 0, 1; rank 0 leads), sixteen warps in four warpgroups:
-//   warp 0      TMA producer: this CTA's A rows [128r, 128r + 128) of the tile
-//               and its half of B (rows [128r, 128r + 128) of the tile's 256),
-//               plus the scale tiles of its A band and of both B bands (each
-//               CTA's TMEM needs the scales of all 256 B rows), into a 5-stage
-//               ring of 38 KB stages;
+//   warps 0, 3  TMA producers: warp 0 this CTA's A rows [128r, 128r + 128) of
+//               the tile and their scale tile, warp 3 its half of B (rows
+//               [128r, 128r + 128) of the tile's 256) and the scale tiles of
+//               both B bands (each CTA's TMEM needs the scales of all 256 B
+//               rows), into a 5-stage ring of 38 KB stages;
 //   warp 1      allocates the pair's TMEM; in the leader it issues, from one
 //               elected lane of the converged warp, tcgen05.mma.cta_group::2
 //               (M = 256, N = 256, K = 64): each CTA's tensor core reads its
@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], 2);             // the activation and the weight producer
             mbar_init(&empty[s], 1);
             mbar_init(&sf_ready[s], 2 * 4);
         }
@@ -178,7 +178,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive_remote(leader_tmem_empty);
+                if (is_leader) mbar_arrive(tmem_empty);          // the leader's own barrier: local arrive
+                else mbar_arrive_remote(leader_tmem_empty);
                 if (use_bias) mbar_arrive(&bias_empty[it & 1]);
             }
 
@@ -245,58 +246,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_st_wait();
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_remote(leader_sf_ready + stage * (uint32_t)sizeof(uint64_t));
+                if (lane == 0) {
+                    if (is_leader) mbar_arrive(&sf_ready[stage]);      // the leader's own barrier: local arrive
+                    else mbar_arrive_remote(leader_sf_ready + stage * (uint32_t)sizeof(uint64_t));
+                }
                 if (++stage == kStages) { stage = 0; phase ^= 1; }
             }
         }
     } else {
         setmaxnreg_dec<kRegsCtl>();
-        if (warp == 0 && lane == 0) {
-            // ------------------------------------------------------ producer --
+        if ((warp == 0 || warp == 3) && lane == 0) {
+            // ----------------------------------------------------- producers --
+            // Two threads per CTA fill the ring, each with its half of every
+            // stage and one arrival on `full` (count 2): warp 0 this CTA's A
+            // rows and their scale tile (after the wait for the preceding
+            // grid, the activation quantizer when launched as its dependent),
+            // warp 3 this CTA's half of B and the scale tiles of both B bands.
+            const bool act_side = warp == 0;
             const uint64_t pol = l2_policy_evict_last();
-            auto issue_w = [&](int stage, const Tile &t, int ks) {
-                const int n_rows = min(kTileN, p.n_out - t.nb * kTileN);
-                const int halves = n_rows > 128 ? 2 : 1;
-                const bool a_here = t.mb * 2 + (int)rank < a_bands;
-                const uint32_t sf_bytes = (uint32_t)min(4, p.num_k64 - ks * 4) * 512;
-                mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes + sf_bytes * ((a_here ? 1 : 0) + halves));
-                tma_load_2d(smem + kOffB + stage * kBBytes, &tmB, &full[stage], ks * kBKBytes,
-                            t.nb * kTileN + (int)rank * kRowsCta, pol);
-                for (int h = 0; h < halves; ++h)
-                    bulk_load(smem + kOffSfb + stage * kSfbBytes + h * 2048,
-                              p.sfb + (t.nb * 2 + h) * p.sfb_band_bytes + (int64_t)ks * 2048, sf_bytes, &full[stage],
-                              pol);
-            };
-            auto issue_a = [&](int stage, const Tile &t, int ks) {
-                const int band_a = t.mb * 2 + (int)rank;
-                const uint32_t sf_bytes = (uint32_t)min(4, p.num_k64 - ks * 4) * 512;
-                tma_load_2d(smem + kOffA + stage * kABytes, &tmA, &full[stage], ks * kBKBytes, band_a * kRowsCta,
-                            pol);
-                if (band_a < a_bands)
-                    bulk_load(smem + kOffSfa + stage * kSfaBytes, p.sfa + band_a * p.sfa_band_bytes + (int64_t)ks * 2048,
-                              sf_bytes, &full[stage], pol);
-            };
-            // Weight side of the first fills before the wait on the preceding
-            // grid (the activation quantizer, when launched as its dependent).
-            int pre = 0;
-            for (int tile = pair_id; tile < num_tiles && pre < kStages; tile += num_pairs) {
-                const Tile t = tile_coord(tile, p.num_m_blk, p.num_n_blk);
-                for (int ks = 0; ks < num_ks && pre < kStages; ++ks) issue_w(pre++, t, ks);
-            }
-            griddep_wait();
-            int stage = 0, fill = 0;
+            if (act_side) griddep_wait();
+            int stage = 0;
             uint32_t phase = 0;
             uint32_t issued_mask = 0, issued_phase = 0;
             bool ok = true;
             for (int tile = pair_id; tile < num_tiles && ok; tile += num_pairs) {
                 const Tile t = tile_coord(tile, p.num_m_blk, p.num_n_blk);
-                for (int ks = 0; ks < num_ks; ++ks, ++fill) {
+                const int band_a = t.mb * 2 + (int)rank;
+                const bool a_here = band_a < a_bands;
+                const int halves = min(kTileN, p.n_out - t.nb * kTileN) > 128 ? 2 : 1;
+                for (int ks = 0; ks < num_ks; ++ks) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, p.err_flag, kErrTimeout, kWaitNs)) {
                         ok = false;
                         break;
                     }
-                    if (fill >= pre) issue_w(stage, t, ks);
-                    issue_a(stage, t, ks);
+                    const uint32_t sf_bytes = (uint32_t)min(4, p.num_k64 - ks * 4) * 512;
+                    if (act_side) {
+                        mbar_arrive_expect_tx(&full[stage], kABytes + (a_here ? sf_bytes : 0));
+                        tma_load_2d(smem + kOffA + stage * kABytes, &tmA, &full[stage], ks * kBKBytes, band_a * kRowsCta,
+                                    pol);
+                        if (a_here)
+                            bulk_load(smem + kOffSfa + stage * kSfaBytes,
+                                      p.sfa + band_a * p.sfa_band_bytes + (int64_t)ks * 2048, sf_bytes, &full[stage], pol);
+                    } else {
+                        mbar_arrive_expect_tx(&full[stage], kBBytes + sf_bytes * halves);
+                        tma_load_2d(smem + kOffB + stage * kBBytes, &tmB, &full[stage], ks * kBKBytes,
+                                    t.nb * kTileN + (int)rank * kRowsCta, pol);
+                        for (int h = 0; h < halves; ++h)
+                            bulk_load(smem + kOffSfb + stage * kSfbBytes + h * 2048,
+                                      p.sfb + (t.nb * 2 + h) * p.sfb_band_bytes + (int64_t)ks * 2048, sf_bytes,
+                                      &full[stage], pol);
+                    }
                     issued_mask |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == kStages) { stage = 0; phase ^= 1; }

@@ -1,7 +1,8 @@
-"""Parity of the CTA-pair GEMM kernel (tcgen05 cta_group::2), which the library
-uses for m > 128 when NVFP4_GEMM_PAIR=1 is set before it loads.  The GEMM and
+"""Parity of the one-CTA GEMM kernel at m > 128, where the library normally
+uses the CTA-pair kernel (tcgen05 cta_group::2).  NVFP4_GEMM_ONE_CTA=1, set
+before the library loads, keeps every GEMM on the one-CTA kernel; the GEMM and
 linear tests run in a child process with that setting, so both kernels stay
-checked against the oracle."""
+checked against the oracle at every size."""
 import os
 import subprocess
 import sys
@@ -13,8 +14,8 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def test_pair_kernel_passes_gemm_parity():
-    env = dict(os.environ, NVFP4_GEMM_PAIR="1")
+def test_one_cta_kernel_passes_gemm_parity():
+    env = dict(os.environ, NVFP4_GEMM_ONE_CTA="1")
     cmd = [sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider",
            os.path.join(ROOT, "tests", "test_gpu_gemm.py"),
            os.path.join(ROOT, "tests", "test_gpu_linear.py") + "::test_llama_shapes",
