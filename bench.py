@@ -63,6 +63,15 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--case", choices=["quant", "gemm", "linear"],
+                    help="run one kernel on synthetic data a few times and exit (for ncu captures): "
+                         "--m/--k/--n/--bs choose the shape, --steps the launches")
+    ap.add_argument("--k", type=int, default=4096)
+    ap.add_argument("--n", type=int, default=4096)
+    ap.add_argument("--bs", type=int, default=0, help="--case: transform block size (0 = none)")
+    ap.add_argument("--suite", action="store_true",
+                    help="instead of the headline line: one JSON line per layer problem of every workload "
+                         "(Llama/Qwen/padded-K/transform) and per point of the quantization sweep")
     a = ap.parse_args(argv)
     a.warmup = max(a.warmup, 3)
     return a
@@ -509,6 +518,93 @@ def run_sweep(args, rank, dev, stream):
     return out
 
 
+def _cold_timer(torch, dev, iters: int = 15, warm: int = 3):
+    """Median CUDA-event time of fn() with a clean, cold L2 before every launch
+    (a 256 MB read evicts what the previous launch left behind)."""
+    cold = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
+
+    def timed(fn) -> float:
+        for _ in range(warm):
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+        for e0, e1 in evs:
+            cold.sum()
+            e0.record()
+            fn()
+            e1.record()
+        torch.cuda.synchronize()
+        return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs) / 1e3
+    return timed
+
+
+def run_suite(args, dev):
+    """Every layer problem of the workloads, timed kernel by kernel with a cold
+    L2: the activation quantizer (with the block-diagonal transform where the
+    workload has one), the GEMM on pre-quantized operands, and nvfp4_linear end
+    to end; then the quantizer bandwidth sweep.  Yields one dict per row."""
+    import torch
+
+    import nvfp4_quantized_linear_gb300 as nv
+    from nvfp4_quantized_linear_gb300 import synthetic as syn
+    nv.build()
+    peaks, _ = load_peaks()
+    fp4_peak = peaks["bf16_tflops_sustained"] * FP4_OVER_BF16
+    hbm = peaks["hbm_gbs"]
+    stream = torch.cuda.current_stream().cuda_stream
+    timed = _cold_timer(torch, dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+
+    problems = syn.llama() + syn.qwen() + syn.padded() + syn.transform_fused()
+    for p in problems:
+        L = syn.make_layer(p, device=dev)
+        gs_x, gs_w, alpha = (torch.tensor([v], **f32) for v in (L.gs_x, L.gs_w, L.alpha))
+        w_fp4, w_sf = nv.prepare_weight(L.w, gs_w)
+        L.w = None
+        ws = torch.empty(nv.nvfp4_linear_workspace_bytes(p.m, p.k, p.n), dtype=torch.uint8, device=dev)
+        kp = nv.padded_k(p.k)
+        a_fp4 = ws[:p.m * kp // 2]
+        a_sf = ws[(p.m * kp // 2 + 255) // 256 * 256:]
+        out = torch.empty((p.m, p.n_keep), dtype=torch.bfloat16, device=dev)
+        t, bs = L.t, p.bs
+
+        def quant():
+            nv.nvfp4_quant_act(L.x, p.m, p.k, p.k, gs_x, t, bs, a_fp4, a_sf, stream)
+
+        def gemm():
+            nv.nvfp4_gemm(a_fp4, a_sf, p.m, w_fp4, w_sf, p.n, p.n_keep, p.k, alpha, L.bias, out, p.n_keep, stream)
+
+        def linear():
+            nv.nvfp4_linear(L.x, p.m, p.k, p.k, gs_x, t, bs, w_fp4, w_sf, p.n, p.n_keep, alpha, L.bias, out,
+                            p.n_keep, ws, ws.numel(), stream)
+
+        tq, tg, tl = timed(quant), timed(gemm), timed(linear)
+        nv.nvfp4_device_error()
+        qb, gb = quant_bytes(p.m, p.k), gemm_bytes(p)
+        yield {"suite": p.workload, "layer": p.name, "m": p.m, "k": p.k, "n": p.n_keep, "bs": bs,
+               "bias": p.bias,
+               "quant_us": round(tq * 1e6, 2), "quant_gbs": round(qb / tq / 1e9, 1),
+               "quant_frac_hbm": round(qb / tq / 1e9 / hbm, 4),
+               "gemm_us": round(tg * 1e6, 2), "gemm_tflops": round(p.flops / tg / 1e12, 1),
+               "gemm_frac_fp4": round(p.flops / tg / 1e12 / fp4_peak, 4),
+               "gemm_gbs": round(gb / tg / 1e9, 1), "gemm_frac_hbm": round(gb / tg / 1e9 / hbm, 4),
+               "linear_us": round(tl * 1e6, 2), "linear_tflops": round(p.flops / tl / 1e12, 1)}
+        del L, w_fp4, w_sf, ws, a_fp4, a_sf, out
+        torch.cuda.empty_cache()
+
+    for m, k, seed in syn.quant_sweep():
+        x = syn.bf16_normal((m, k), 1.0, seed, device=dev)
+        gs = torch.tensor([syn.global_scale(x)], **f32)
+        x_fp4, x_sf = nv.quant_act(x, gs)
+        tq = timed(lambda: nv.nvfp4_quant_act(x, m, k, k, gs, None, 0, x_fp4, x_sf, stream))
+        nv.nvfp4_device_error()
+        qb = quant_bytes(m, k)
+        yield {"suite": "quant_sweep", "m": m, "k": k, "quant_us": round(tq * 1e6, 2),
+               "quant_gbs": round(qb / tq / 1e9, 1), "quant_frac_hbm": round(qb / tq / 1e9 / hbm, 4),
+               "bytes": qb}
+        del x, x_fp4, x_sf
+        torch.cuda.empty_cache()
+
+
 def run_reference(args, rank, world):
     """The reference arm: the CPU oracle, as it stands, on a bounded sample of
     the same workload per step (rank 0 only)."""
@@ -533,14 +629,62 @@ def run_reference(args, rank, world):
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_case(args):
+    """One kernel on a synthetic N(0, 1) activation [M, K] (transformed by a
+    random bs x bs Hadamard block when --bs > 0) and an N(0, 0.02) weight
+    [N, K], launched --steps times; prints 'ok'."""
+    import torch
+
+    import nvfp4_quantized_linear_gb300 as nv
+    from nvfp4_quantized_linear_gb300 import synthetic as syn
+    nv.build()
+    dev = torch.device("cuda", 0)
+    m, k, n, bs = args.m, args.k, args.n, args.bs
+    x = syn.bf16_normal((m, k), 1.0, 3, device=dev)
+    t = syn.random_hadamard_transform(bs, seed=bs).to(dev) if bs else None
+    gs = torch.tensor([30.0], dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream().cuda_stream
+    x_fp4, x_sf = nv.quant_act(x, gs, t, bs)
+    if args.case != "quant":
+        w = syn.bf16_normal((n, k), 0.02, 4, device=dev)
+        w_fp4, w_sf = nv.prepare_weight(w, torch.tensor([syn.global_scale(w)], dtype=torch.float32, device=dev))
+        alpha = torch.tensor([1e-3], dtype=torch.float32, device=dev)
+        out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(nv.nvfp4_linear_workspace_bytes(m, k, n), dtype=torch.uint8, device=dev)
+    for _ in range(args.steps):
+        if args.case == "quant":
+            nv.nvfp4_quant_act(x, m, k, k, gs, t, bs, x_fp4, x_sf, stream)
+        elif args.case == "gemm":
+            nv.nvfp4_gemm(x_fp4, x_sf, m, w_fp4, w_sf, n, n, k, alpha, None, out, n, stream)
+        else:
+            nv.nvfp4_linear(x, m, k, k, gs, t, bs, w_fp4, w_sf, n, n, alpha, None, out, n, ws, ws.numel(), stream)
+    torch.cuda.synchronize()
+    nv.nvfp4_device_error()
+    print("ok")
+
+
 def main(argv=None):
     args = parse_args(argv)
     rank, world, local_rank = dist_env()
+    if args.case:
+        run_case(args)
+        return
     if world > 1 and args.impl == "ours":
         import torch
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if args.suite:
+        import torch
+        dev = torch.device("cuda", local_rank)
+        torch.cuda.set_device(dev)
+        sampler = ClockSampler(local_rank)
+        with sampler:
+            for row in run_suite(args, dev):
+                print(json.dumps(row), flush=True)
+        print(json.dumps({"suite": "clocks", **sampler.summary(), "l2": "256 MB read before every launch; "
+                          "median of 15 launches after 3 warm-up"}), flush=True)
+        return
     if args.impl == "reference":
         res = run_reference(args, rank, world)
     else:

@@ -139,13 +139,27 @@ nvfp4_status nvfp4_prepare_weight(const void *w_bf16, int64_t n, int64_t k, int6
  *   transform_bf16  in   NULL (bs = 0) for none, else a bs x bs bf16 matrix T,
  *                        row-major, 1/sqrt(bs) already folded in; bs in
  *                        {16,32,64,128} and bs must divide k.  Then every bs-wide
- *                        block of a row is replaced by y = bf16(x_block * T),
- *                        accumulated in fp32 in index order, before quantizing.
+ *                        block of a row is replaced by y = bf16(x_block * T)
+ *                        before quantizing: the exact bf16 x bf16 products are
+ *                        summed in fp32 on the tensor cores, in their own
+ *                        order, and rounded to bf16 once.
  *   x_fp4           out  nvfp4_packed_bytes(m, k) bytes
  *   x_sf            out  nvfp4_scale_bytes(m, k) bytes                        */
 nvfp4_status nvfp4_quant_act(const void *x_bf16, int64_t m, int64_t k, int64_t ldx,
                              const float *gs_dev, const void *transform_bf16, int bs,
                              uint8_t *x_fp4, uint8_t *x_sf, nvfp4_stream_t stream);
+
+/* nvfp4_quant_act with a transform (transform_bf16 non-NULL), which also
+ * writes the bf16 transform result y that the codes and scales were computed
+ * from: y_bf16 (out, device, 16-byte aligned) is [m, k] bf16 with row stride
+ * k, and must not overlap any other argument.  The codes are then a function
+ * of y alone, so a checker can requantize y and compare bit for bit, and
+ * compare y itself with x * blockdiag(T).  Same kernel and same x_fp4/x_sf
+ * bytes as nvfp4_quant_act; the extra output costs 2 bytes per element. */
+nvfp4_status nvfp4_quant_act_export_y(const void *x_bf16, int64_t m, int64_t k, int64_t ldx,
+                                      const float *gs_dev, const void *transform_bf16, int bs,
+                                      uint8_t *x_fp4, uint8_t *x_sf, void *y_bf16,
+                                      nvfp4_stream_t stream);
 
 /* Block-scaled FP4 GEMM with the fused epilogue (torch-backend page:
  * torch._scaled_mm, then * alpha, slice_nvfp4_output, + bias):

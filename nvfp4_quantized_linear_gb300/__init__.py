@@ -22,7 +22,7 @@ __all__ = [
     "NVFP4_OK", "Nvfp4Error", "library_path", "load_library", "build",
     "nvfp4_abi_version", "nvfp4_is_supported", "nvfp4_last_error_string", "nvfp4_device_error",
     "nvfp4_packed_bytes", "nvfp4_scale_bytes", "nvfp4_linear_workspace_bytes",
-    "nvfp4_prepare_weight", "nvfp4_quant_act", "nvfp4_gemm", "nvfp4_linear", "nvfp4_linear_noalloc",
+    "nvfp4_prepare_weight", "nvfp4_quant_act", "nvfp4_quant_act_export_y", "nvfp4_gemm", "nvfp4_linear", "nvfp4_linear_noalloc",
     "padded_k", "scale_shape",
 ]
 
@@ -48,6 +48,7 @@ EXPORTS = [
     ("nvfp4_linear_workspace_bytes", _SZ, [_I64, _I64, _I64]),
     ("nvfp4_prepare_weight", _I32, [_P, _I64, _I64, _I64, _P, _P, _P, _P]),
     ("nvfp4_quant_act", _I32, [_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _P]),
+    ("nvfp4_quant_act_export_y", _I32, [_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _P, _P]),
     ("nvfp4_gemm", _I32, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _P, _P, _I64, _P]),
     ("nvfp4_linear", _I32, [_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _I64, _I64, _P, _P, _P, _I64,
                             _P, _SZ, _P]),
@@ -170,6 +171,12 @@ def nvfp4_prepare_weight(w, n: int, k: int, ldw: int, w_gs, w_fp4, w_sf, stream=
 def nvfp4_quant_act(x, m: int, k: int, ldx: int, gs, transform, bs: int, x_fp4, x_sf, stream=None) -> None:
     _check(load_library().nvfp4_quant_act(_ptr(x), m, k, ldx, _ptr(gs), _ptr(transform), bs, _ptr(x_fp4),
                                           _ptr(x_sf), _stream(stream)))
+
+
+def nvfp4_quant_act_export_y(x, m: int, k: int, ldx: int, gs, transform, bs: int, x_fp4, x_sf, y,
+                             stream=None) -> None:
+    _check(load_library().nvfp4_quant_act_export_y(_ptr(x), m, k, ldx, _ptr(gs), _ptr(transform), bs, _ptr(x_fp4),
+                                                   _ptr(x_sf), _ptr(y), _stream(stream)))
 
 
 def nvfp4_gemm(a_fp4, a_sf, m: int, w_fp4, w_sf, n_w: int, n_out: int, k: int, alpha, bias, out, ldo: int,

@@ -171,6 +171,8 @@ nvfp4::QuantParams quant_params(const void *x, int64_t m, int64_t k, int64_t ldx
     p.sf = x_sf;
     p.t = static_cast<const uint16_t *>(t);
     p.bs = t ? bs : 0;
+    p.err_flag = nullptr;
+    p.y_out = nullptr;
     return p;
 }
 
@@ -183,10 +185,16 @@ nvfp4_status launch_status(cudaError_t e, const char *what)
     return ok();
 }
 
-nvfp4_status run_quant(const nvfp4::QuantParams &p, int num_sms, cudaStream_t s)
+nvfp4_status run_quant(nvfp4::QuantParams p, int num_sms, cudaStream_t s)
 {
-    if (p.bs)
-        return launch_status(nvfp4::launch_quant_transform(p, num_sms, s), "transform-quantize kernel");
+    if (p.bs) {
+        cudaError_t e = nvfp4::device_error_word(&p.err_flag);
+        if (e != cudaSuccess) return launch_status(e, "transform-quantize kernel (error word)");
+        const char *why = nullptr;
+        e = nvfp4::launch_quant_transform(p, num_sms, s, &why);
+        if (why) return fail(NVFP4_ERR_CUDA, "%s", why);
+        return launch_status(e, "transform-quantize kernel");
+    }
     return launch_status(nvfp4::launch_quant(p, num_sms, s), "quantize kernel");
 }
 
@@ -418,6 +426,28 @@ nvfp4_status nvfp4_quant_act(const void *x_bf16, int64_t m, int64_t k, int64_t l
     if ((st = current_device(&num_sms)) != NVFP4_OK) return st;
     return run_quant(quant_params(x_bf16, m, k, ldx, gs_dev, transform_bf16, bs, x_fp4, x_sf), num_sms,
                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status nvfp4_quant_act_export_y(const void *x_bf16, int64_t m, int64_t k, int64_t ldx, const float *gs_dev,
+                                      const void *transform_bf16, int bs, uint8_t *x_fp4, uint8_t *x_sf, void *y_bf16,
+                                      nvfp4_stream_t stream)
+{
+    nvfp4_status st = check_quant_args(x_bf16, m, k, ldx, gs_dev, transform_bf16, bs, x_fp4, x_sf, "x");
+    if (st != NVFP4_OK) return st;
+    if (transform_bf16 == nullptr) return fail(NVFP4_ERR_INVALID_ARG, "y export needs a transform");
+    if (m == 0) return ok();
+    if (y_bf16 == nullptr) return fail(NVFP4_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned16(y_bf16)) return fail(NVFP4_ERR_ALIGNMENT, "y must be 16-byte aligned");
+    Range outs[3] = {range(x_fp4, nvfp4_packed_bytes(m, k), "x_fp4"), range(x_sf, nvfp4_scale_bytes(m, k), "x_sf"),
+                     range(y_bf16, (size_t)m * (size_t)k * 2, "y")};
+    Range ins[3] = {range2d(x_bf16, m, k, ldx, "x"), range(gs_dev, 4, "gs"),
+                    range(transform_bf16, (size_t)bs * bs * 2, "transform")};
+    if ((st = check_aliases(outs, 3, ins, 3)) != NVFP4_OK) return st;
+    int num_sms = 0;
+    if ((st = current_device(&num_sms)) != NVFP4_OK) return st;
+    nvfp4::QuantParams p = quant_params(x_bf16, m, k, ldx, gs_dev, transform_bf16, bs, x_fp4, x_sf);
+    p.y_out = static_cast<uint16_t *>(y_bf16);
+    return run_quant(p, num_sms, reinterpret_cast<cudaStream_t>(stream));
 }
 
 nvfp4_status nvfp4_prepare_weight(const void *w_bf16, int64_t n, int64_t k, int64_t ldw, const float *w_gs_dev,

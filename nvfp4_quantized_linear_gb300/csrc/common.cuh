@@ -37,6 +37,8 @@ struct QuantParams {
     uint8_t *sf;           // tiled [mp, nbp]
     const uint16_t *t;     // transform (bf16 bits) or nullptr
     int32_t bs;
+    unsigned int *err_flag;  // device error word (transform kernel's bounded waits)
+    uint16_t *y_out;         // nullptr, or [m, k] bf16: the transform result (row stride k)
 };
 
 constexpr int kMaxSplits = 16;       // split-K ranges at most
@@ -65,7 +67,7 @@ struct GemmParams {
 
 // Launchers (return a cudaError_t; no host synchronisation).
 cudaError_t launch_quant(const QuantParams &p, int num_sms, cudaStream_t s);
-cudaError_t launch_quant_transform(const QuantParams &p, int num_sms, cudaStream_t s);
+cudaError_t launch_quant_transform(const QuantParams &p, int num_sms, cudaStream_t s, const char **why);
 // dependent = true launches the GEMM as a programmatic dependent of the
 // preceding kernel, which must be the quantizer of its activation operand:
 // the GEMM's weight-side loads then start before that kernel has finished.

@@ -1,4 +1,5 @@
-// Pieces shared by the two GEMM kernels (one CTA per tile, and CTA pairs).
+// Pieces shared by the tensor-core kernels (the two GEMMs and the transform
+// quantizer): tile order, tensor-map builders.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -80,6 +81,23 @@ inline bool make_output_map(CUtensorMap *map, void *base, uint64_t n_out, uint64
     cuuint32_t estr[2] = {1, 1};
     return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base, dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D map over bf16 rows [rows, cols] (row stride ld elements) with boxes of
+// 64 columns x 128 rows, 128-byte swizzle (the K-major operand layout of a
+// kind::f16 MMA), zero fill outside the tensor.  Requires a 16-B aligned base
+// and ld % 8 == 0.
+inline bool make_bf16_rows_map(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint64_t ld)
+{
+    auto encode = tensor_map_encoder();
+    if (encode == nullptr) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {ld * 2};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t estr[2] = {1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -235,6 +235,19 @@ __device__ __forceinline__ void tc_mma_nvf4(uint32_t d_tmem, uint64_t a_desc, ui
         : "memory");
 }
 
+// D(tmem) (+)= A(smem) * B(smem)^T with bf16 operands, fp32 accumulation
+// (kind::f16, K = 16).
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Each thread of the warp reads 32 consecutive 32-bit columns of its own TMEM
 // lane (lane = warp's quarter * 32 + laneid).
 __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32])
@@ -386,6 +399,17 @@ __host__ __device__ constexpr uint32_t idesc_nvf4(uint32_t M, uint32_t N)
            | (1u << 10)           // B format: E2M1
            | ((N >> 3) << 17)     // N / 8
            | ((M >> 4) << 24);    // M / 16   (scale format bit 23 = 0: UE4M3; scale ids 0)
+}
+
+// Instruction descriptor of the kind::f16 MMA: bf16 x bf16, fp32 accumulate,
+// both operands K-major, dense, shape M x N (K = 16).
+__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N)
+{
+    return (1u << 4)              // D format: F32
+           | (1u << 7)            // A format: BF16
+           | (1u << 10)           // B format: BF16
+           | ((N >> 3) << 17)     // N / 8
+           | ((M >> 4) << 24);    // M / 16
 }
 
 // ------------------------------------------------- CTA pairs (cta_group::2) ----

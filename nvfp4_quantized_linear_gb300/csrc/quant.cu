@@ -14,6 +14,7 @@
 #include <cuda_fp16.h>
 
 #include "common.cuh"
+#include "gemm_common.cuh"
 #include "ptx.cuh"
 #include "scale_math.cuh"
 
@@ -166,107 +167,266 @@ __global__ void __launch_bounds__(256) quant_kernel(const QuantParams p)
 }
 
 // ---------------------------------------------------------------------------
-// Transform + quantizer.  A CTA tile is 32 rows x 256 columns.  The tile is
-// staged in shared memory (row stride 129 words: conflict-free column reads),
-// T is held in shared memory as fp32.  Thread (warp w, lane l) computes, for
-// row l, the 16 outputs of units w and w+8 (a unit = 16 consecutive columns =
-// one scale block): y_j = bf16(acc_j), acc_j an fp32 fused multiply-add chain
-// over i = 0..bs-1 in index order, then quantizes the 16 values in-thread.
-constexpr int kXRowWords = 129;
+// Transform + quantizer on the tensor cores.  y = x * blockdiag(T) is a dense
+// contraction per bs-block, so each 128-row x 128-column tile of x goes
+// through tcgen05.mma (kind::f16: bf16 operands, fp32 accumulation in TMEM):
+// for every bs-block g of the tile, bs/16 MMAs of M = 128, N = bs, K = 16 give
+//     D[:, g*bs : (g+1)*bs] = X[:, g*bs : (g+1)*bs] * T,
+// always 8 MMAs per tile.  The bf16 x bf16 products are exact in fp32; the
+// sum is accumulated in fp32 by the tensor core and rounded to bf16 once, in
+// the epilogue, which then quantizes y exactly as the plain quantizer does.
+//
+// One CTA per SM, persistent over the tiles (column tiles of a 128-row band
+// consecutive):
+//   warp 0      lane 0: TMA loads of the x tile (two boxes of 64 columns x
+//               128 rows, 128-byte swizzle, zero fill past m and k) into a
+//               4-stage ring;
+//   warp 1      allocates the 256 TMEM columns (two 128-column accumulators);
+//               an elected lane issues each tile's MMAs and commits;
+//   warps 2..9  epilogue, two per TMEM lane quarter (64 columns each): read
+//               the accumulator, hand it back, round to bf16, block scale,
+//               E2M1 codes, stores (packed rows < m, scale rows < mp; and y
+//               itself when the caller asks for it).
+// T^T is the B operand: row n holds column n of T, in the same swizzled
+// K-major form; K-chunk c (rows 64c .. 64c+63 of T) at byte c * bs * 128.
+// Every mbarrier wait is bounded (about 2 s); on expiry the kernel raises the
+// device error word and exits.
+constexpr int kXfRows = 128;                               // tile rows = MMA M
+constexpr int kXfCols = 128;                               // tile columns
+constexpr int kXfStages = 4;
+constexpr uint32_t kXfBoxBytes = 128 * 128;                // 128 rows x 64 bf16
+constexpr uint32_t kXfStageBytes = 2 * kXfBoxBytes;
+constexpr uint32_t kXfOffT = kXfStages * kXfStageBytes;    // T^T: up to 2 K-chunks of 128 rows
+constexpr uint32_t kXfOffBar = kXfOffT + 2 * kXfBoxBytes;
+constexpr uint32_t kXfSmemBytes = kXfOffBar + 256 + 1024;  // barriers + alignment slack
+constexpr int kXfEpiWarp0 = 2;
+constexpr int kXfEpiCols = 64;                             // columns of a tile per epilogue warp
+constexpr int kXfEpiWarps = 4 * (kXfCols / kXfEpiCols);    // kXfCols / kXfEpiCols per TMEM lane quarter
+constexpr int kXfUnits = kXfEpiCols / 16;                  // scale blocks per thread and tile
+constexpr int kXfThreads = 32 * (kXfEpiWarp0 + kXfEpiWarps);
+constexpr uint32_t kXfTmemCols = 2 * kXfCols;
+constexpr uint64_t kXfWaitNs = 2000000000ull;
+static_assert(kXfSmemBytes <= 232448, "shared memory budget");
 
-__global__ void __launch_bounds__(256) quant_transform_kernel(const QuantParams p)
+__device__ __forceinline__ float round_bf16(float f) { return __bfloat162float(__float2bfloat16_rn(f)); }
+
+__global__ void __launch_bounds__(kXfThreads, 1)
+    quant_transform_kernel(const __grid_constant__ CUtensorMap tmX, const QuantParams p)
 {
-    extern __shared__ float smem_f[];
-    const int bs = p.bs;
-    float *sT = smem_f;
-    uint32_t *sX = reinterpret_cast<uint32_t *>(smem_f + bs * bs);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0) griddep_launch_dependents();    // as in quant_kernel
-
+    extern __shared__ uint8_t xf_smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(xf_smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kXfOffBar);
+    uint64_t *empty = full + kXfStages;
+    uint64_t *tmem_full = empty + kXfStages;      // [2]
+    uint64_t *tmem_empty = tmem_full + 2;         // [2]
+    uint64_t *mma_done = tmem_empty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
     __shared__ float inv_tab[128];
-    for (int i = tid; i < bs * bs; i += 256) sT[i] = __uint_as_float((uint32_t)p.t[i] << 16);
-    const float gs = __ldg(p.gs);
-    fill_inv_table(inv_tab, gs);                           // visible after the first tile's barrier
-    const int segs = (p.kp + 255) >> 8;
-    const int64_t tiles = (int64_t)(p.mp / 32) * segs;
-    const int64_t out_ld = p.kp >> 1;
 
-    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
-        const int64_t r0 = (tile / segs) * 32;
-        const int kseg = (int)(tile % segs) * 256;
-        __syncthreads();                                   // previous tile fully consumed
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-            const int idx = it * 256 + tid;
-            const int rr = idx >> 5, ch = idx & 31;
-            const int64_t r = r0 + rr;
-            const int k = kseg + ch * 8;
-            uint4 w = make_uint4(0, 0, 0, 0);
-            if (r < p.m && k < p.k) w = ld_stream_v4(p.x + r * p.ldx + k);   // k % 16 == 0: whole chunk valid
-            uint32_t *dst = sX + rr * kXRowWords + ch * 4;
-            dst[0] = w.x; dst[1] = w.y; dst[2] = w.z; dst[3] = w.w;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int bs = p.bs;
+    if (threadIdx.x == 0) {
+        griddep_launch_dependents();              // as in quant_kernel
+        for (int s = 0; s < kXfStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
         }
-        __syncthreads();
-
-        const int64_t r = r0 + lane;
-#pragma unroll 1
-        for (int uu = 0; uu < 2; ++uu) {
-            const int u = warp + uu * 8;
-            const int c0 = kseg + u * 16;
-            if (c0 >= p.kp) continue;                      // uniform across the warp
-            float acc[16];
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tmem_full[b], 1);
+            mbar_init(&tmem_empty[b], kXfEpiWarps);
+        }
+        mbar_init(mma_done, 1);
+        fence_mbarrier_init();
+        prefetch_tensormap(&tmX);
+    }
+    // T^T into shared memory: element T[i][n] -> row n, K index i, written
+    // where the 128-byte swizzle puts it (16-byte chunk index XOR row % 8).
+    // Each thread first loads its 16-byte pieces of T (8 consecutive n of one
+    // row i; T is 16-byte aligned), all loads in flight at once, then scatters.
+    uint8_t *sT = smem + kXfOffT;
+    {
+        constexpr int kPieces = (128 * 128 / 8 + kXfThreads - 1) / kXfThreads;
+        const int lg = 31 - __clz(bs);                    // bs = 2^lg
+        const int pieces = bs * bs / 8;
+        uint4 tv[kPieces];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
-            if (c0 < p.k) {
-                const int blk = (u * 16) / bs * bs;         // first column of the bs-block in this segment
-                const int j0 = (u * 16) % bs;
-                const uint32_t *xr = sX + lane * kXRowWords + (blk >> 1);
-#pragma unroll 2
-                for (int i = 0; i < bs; i += 2) {
-                    const uint32_t xw = xr[i >> 1];
-                    const float x0 = bf16_lo(xw), x1 = bf16_hi(xw);
-                    const float4 *t0 = reinterpret_cast<const float4 *>(sT + i * bs + j0);
-                    const float4 *t1 = reinterpret_cast<const float4 *>(sT + (i + 1) * bs + j0);
+        for (int u = 0; u < kPieces; ++u) {
+            const int c = (int)threadIdx.x + u * kXfThreads;
+            if (c < pieces) tv[u] = __ldg(reinterpret_cast<const uint4 *>(p.t) + c);
+        }
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float4 a = t0[q];
-                        acc[4 * q + 0] = __fmaf_rn(x0, a.x, acc[4 * q + 0]);
-                        acc[4 * q + 1] = __fmaf_rn(x0, a.y, acc[4 * q + 1]);
-                        acc[4 * q + 2] = __fmaf_rn(x0, a.z, acc[4 * q + 2]);
-                        acc[4 * q + 3] = __fmaf_rn(x0, a.w, acc[4 * q + 3]);
-                    }
+        for (int u = 0; u < kPieces; ++u) {
+            const int c = (int)threadIdx.x + u * kXfThreads;
+            if (c < pieces) {
+                const int i = c >> (lg - 3);
+                const int n0 = (c & ((bs >> 3) - 1)) << 3;
+                const uint32_t kb = (uint32_t)(i & 63) * 2;
+                const uint32_t row0 = (uint32_t)(i >> 6) * bs * 128 + (kb & 15);
+                const uint32_t w[4] = {tv[u].x, tv[u].y, tv[u].z, tv[u].w};
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float4 a = t1[q];
-                        acc[4 * q + 0] = __fmaf_rn(x1, a.x, acc[4 * q + 0]);
-                        acc[4 * q + 1] = __fmaf_rn(x1, a.y, acc[4 * q + 1]);
-                        acc[4 * q + 2] = __fmaf_rn(x1, a.z, acc[4 * q + 2]);
-                        acc[4 * q + 3] = __fmaf_rn(x1, a.w, acc[4 * q + 3]);
-                    }
+                for (int q = 0; q < 8; ++q) {
+                    const int n = n0 + q;
+                    *reinterpret_cast<uint16_t *>(sT + row0 + n * 128 + (((kb >> 4) ^ (n & 7)) << 4)) =
+                        (uint16_t)(w[q >> 1] >> ((q & 1) * 16));
                 }
             }
-            float y0[8], y1[8];
-            float amax = 0.0f;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                y0[j] = __bfloat162float(__float2bfloat16_rn(acc[j]));
-                y1[j] = __bfloat162float(__float2bfloat16_rn(acc[8 + j]));
-                amax = fmaxf(amax, fmaxf(fabsf(y0[j]), fabsf(y1[j])));
-            }
-            float inv;
-            const uint32_t sf = block_scale_tab(amax, gs, inv_tab, inv);
-            if (r < p.m) {
-                uint2 pk;
-                pk.x = quant8(y0, inv);
-                pk.y = quant8(y1, inv);
-                *reinterpret_cast<uint2 *>(p.out + r * out_ld + (c0 >> 1)) = pk;
-            }
-            const int cb = c0 >> 4;
-            p.sf[sf_offset(r, cb, p.nbp)] = (uint8_t)sf;
-            if (cb == p.nb - 1)                             // zero the column padding of this row
-                for (int c = p.nb; c < p.nbp; ++c) p.sf[sf_offset(r, c, p.nbp)] = 0;
         }
     }
+    fence_proxy_async_shared();                   // the MMAs read T^T through the async proxy
+    const float gs = __ldg(p.gs);
+    fill_inv_table(inv_tab, gs);
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kXfTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    const int n_ct = (p.nbp * 16 + kXfCols - 1) / kXfCols;   // covers every scale column
+    const int num_tiles = (p.mp / kXfRows) * n_ct;
+
+    if (warp >= kXfEpiWarp0) {
+        // ---------------------------------------------------------- epilogue --
+        const int q = warp & 3;
+        const int h = (warp - kXfEpiWarp0) >> 2;
+        const int64_t out_ld = p.kp >> 1;
+        int it = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+            const int b = it & 1;
+            if (!__all_sync(~0u, mbar_wait(&tmem_full[b], (uint32_t)(it >> 1) & 1u, p.err_flag, kErrTimeout,
+                                           kXfWaitNs)))
+                break;
+            tc_fence_after_sync();
+            const uint32_t src = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * kXfCols + h * kXfEpiCols);
+            uint32_t v[kXfEpiCols];
+#pragma unroll
+            for (int c = 0; c < kXfEpiCols / 32; ++c)
+                tmem_ld_32cols(src + 32 * c, reinterpret_cast<uint32_t(&)[32]>(v[32 * c]));
+#pragma unroll
+            for (int c = 0; c < kXfEpiCols / 32; ++c) tmem_ld_wait_regs(reinterpret_cast<uint32_t(&)[32]>(v[32 * c]));
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tmem_empty[b]);
+
+            const int rb = tile / n_ct, ct = tile - rb * n_ct;
+            const int64_t r = (int64_t)rb * kXfRows + q * 32 + lane;
+            const int c0 = ct * kXfCols + h * kXfEpiCols;
+            uint32_t pk[2 * kXfUnits];
+            uint32_t sfw = 0;
+#pragma unroll
+            for (int u = 0; u < kXfUnits; ++u) {
+                const uint32_t *a = v + 16 * u;
+                float y0[8], y1[8];
+                float amax = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    y0[j] = round_bf16(__uint_as_float(a[j]));
+                    y1[j] = round_bf16(__uint_as_float(a[8 + j]));
+                    amax = fmaxf(amax, fmaxf(fabsf(y0[j]), fabsf(y1[j])));
+                }
+                float inv;
+                const uint32_t sf = block_scale_tab(amax, gs, inv_tab, inv);
+                pk[2 * u] = quant8(y0, inv);
+                pk[2 * u + 1] = quant8(y1, inv);
+                sfw |= sf << (8 * u);
+                if (p.y_out != nullptr && r < p.m && c0 + 16 * u < p.k) {   // k % 16 == 0
+                    uint32_t w[8];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        w[j] = (__float_as_uint(y0[2 * j]) >> 16) | (__float_as_uint(y0[2 * j + 1]) & 0xFFFF0000u);
+                        w[4 + j] = (__float_as_uint(y1[2 * j]) >> 16) | (__float_as_uint(y1[2 * j + 1]) & 0xFFFF0000u);
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.y_out + r * p.k + c0 + 16 * u);
+                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                }
+            }
+            if (r < p.m) {
+                uint8_t *o = p.out + r * out_ld + (c0 >> 1);
+#pragma unroll
+                for (int pr = 0; pr < kXfUnits / 2; ++pr)           // 32 columns = 16 bytes (kp % 32 == 0)
+                    if (c0 + 32 * pr < p.kp)
+                        *reinterpret_cast<uint4 *>(o + 16 * pr) =
+                            make_uint4(pk[4 * pr], pk[4 * pr + 1], pk[4 * pr + 2], pk[4 * pr + 3]);
+            }
+            const int cs = c0 >> 4;                       // columns >= k were zero-filled: codes 0
+            if (cs < p.nbp) {                             // nbp % 4 == 0: the whole group is inside
+                if (kXfUnits == 4)
+                    *reinterpret_cast<uint32_t *>(p.sf + sf_offset(r, cs, p.nbp)) = sfw;
+                else
+                    *reinterpret_cast<uint16_t *>(p.sf + sf_offset(r, cs, p.nbp)) = (uint16_t)sfw;
+            }
+        }
+    } else if (warp == 0) {
+        if (lane == 0) {
+            // --------------------------------------------------------- producer --
+            const uint64_t pol = l2_policy_evict_first();   // x is read once
+            int it = 0;
+            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+                const int stage = it % kXfStages;
+                if (!mbar_wait(&empty[stage], ((uint32_t)(it / kXfStages) & 1u) ^ 1u, p.err_flag, kErrTimeout,
+                               kXfWaitNs))
+                    break;
+                const int rb = tile / n_ct, ct = tile - rb * n_ct;
+                uint8_t *dst = smem + stage * kXfStageBytes;
+                mbar_arrive_expect_tx(&full[stage], kXfStageBytes);
+                tma_load_2d(dst, &tmX, &full[stage], ct * kXfCols, rb * kXfRows, pol);
+                tma_load_2d(dst + kXfBoxBytes, &tmX, &full[stage], ct * kXfCols + 64, rb * kXfRows, pol);
+            }
+            // Every copy issued has landed before the CTA may exit (the last
+            // issue of each stage is its newest phase).
+            for (int j = max(0, it - kXfStages); j < it; ++j)
+                mbar_wait(&full[j % kXfStages], (uint32_t)(j / kXfStages) & 1u, p.err_flag, kErrTimeout, kXfWaitNs);
+        }
+    } else {
+        // ---------------------------------------------------------------- MMA --
+        const bool leader = elect_one();
+        const uint32_t idesc = idesc_bf16(128, (uint32_t)bs);
+        const uint32_t x_base = smem_u32(smem);
+        const uint32_t t_base = smem_u32(sT);
+        int it = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+            const int stage = it % kXfStages;
+            const int b = it & 1;
+            if (!__all_sync(~0u, mbar_wait(&tmem_empty[b], ((uint32_t)(it >> 1) & 1u) ^ 1u, p.err_flag, kErrTimeout,
+                                           kXfWaitNs)))
+                break;
+            if (!__all_sync(~0u, mbar_wait(&full[stage], (uint32_t)(it / kXfStages) & 1u, p.err_flag, kErrTimeout,
+                                           kXfWaitNs)))
+                break;
+            tc_fence_after_sync();
+            if (leader) {
+                const uint32_t d0 = tmem + (uint32_t)(b * kXfCols);
+                const uint32_t xs = x_base + stage * kXfStageBytes;
+                for (int g = 0; g < kXfCols / bs; ++g) {
+                    for (int kk = 0; kk < bs / 16; ++kk) {
+                        // K-step of 16: 32 bytes further into the swizzled 128-byte rows
+                        const int c = g * bs + kk * 16;       // column of the x tile
+                        const int i = kk * 16;                // row of T
+                        const uint32_t a_addr = xs + (uint32_t)(c >> 6) * kXfBoxBytes + (uint32_t)(c & 63) * 2;
+                        const uint32_t b_addr = t_base + (uint32_t)(i >> 6) * bs * 128 + (uint32_t)(i & 63) * 2;
+                        tc_mma_bf16(d0 + (uint32_t)(g * bs), smem_desc_sw128(a_addr), smem_desc_sw128(b_addr), idesc,
+                                    kk != 0);
+                    }
+                }
+                tc_commit(&empty[stage]);
+                tc_commit(&tmem_full[b]);
+            }
+            __syncwarp();
+        }
+        // No MMA may still be running when the TMEM is released.
+        if (leader) tc_commit(mma_done);
+        __syncwarp();
+        mbar_wait(mma_done, 0, p.err_flag, kErrTimeout, kXfWaitNs);
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == 1) tmem_dealloc(tmem, kXfTmemCols);
 }
 
 }  // namespace
@@ -285,25 +445,26 @@ cudaError_t launch_quant(const QuantParams &p, int num_sms, cudaStream_t s)
     return cudaGetLastError();
 }
 
-cudaError_t launch_quant_transform(const QuantParams &p, int num_sms, cudaStream_t s)
+cudaError_t launch_quant_transform(const QuantParams &p, int num_sms, cudaStream_t s, const char **why)
 {
-    const size_t smem = (size_t)p.bs * p.bs * sizeof(float) + 32 * kXRowWords * sizeof(uint32_t);
     static int configured_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
         cudaError_t e = cudaFuncSetAttribute(quant_transform_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)(128 * 128 * sizeof(float) + 32 * kXRowWords * sizeof(uint32_t)));
+                                             (int)kXfSmemBytes);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    const int64_t segs = (p.kp + 255) / 256;
-    const int64_t tiles = (int64_t)(p.mp / 32) * segs;
-    int64_t blocks = tiles;
-    const int64_t cap = (int64_t)num_sms * 2;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
-    quant_transform_kernel<<<(unsigned)blocks, 256, smem, s>>>(p);
+    CUtensorMap tmX;
+    if (!gemm_detail::make_bf16_rows_map(&tmX, p.x, (uint64_t)p.k, (uint64_t)p.m, (uint64_t)p.ldx)) {
+        *why = "cuTensorMapEncodeTiled failed for the activation";
+        return cudaErrorInvalidValue;
+    }
+    const int64_t n_ct = ((int64_t)p.nbp * 16 + kXfCols - 1) / kXfCols;
+    const int64_t tiles = (int64_t)(p.mp / kXfRows) * n_ct;
+    const int grid = (int)(tiles < num_sms ? tiles : num_sms);
+    quant_transform_kernel<<<(unsigned)grid, kXfThreads, kXfSmemBytes, s>>>(tmX, p);
     return cudaGetLastError();
 }
 

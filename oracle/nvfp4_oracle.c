@@ -32,9 +32,8 @@
  *   R-swz    scale tiles of 128 rows x 4 columns, 512 bytes each,
  *            offset(r,c) = ((r/128)*(Cp/4) + c/4)*512 + (r%32)*16 + ((r%128)/32)*4 + c%4,
  *            rows padded to 128 and columns to 4 with zero bytes.
- *   R-xform  y[j] = bf16_rne(acc), acc an fp32 accumulator that takes the bs
- *            products x[i]*T[i][j] in index order i = 0..bs-1, one fused
- *            multiply-add (single rounding) per step, starting from +0.
+ *   R-xform  y[j] = bf16_rne(sum_i x[i]*T[i][j]) of the exact sum (no
+ *            intermediate rounding; an exact zero sum gives +0).
  *   R-gemm   out[m,n] = alpha * sum_k deq(A)[m,k]*deq(B)[n,k] + bias[n] in FP64,
  *            where deq(q) = e2m1(q) * e4m3(sf) (the global scales live in alpha).
  *
@@ -225,23 +224,106 @@ void oracle_unswizzle(const uint8_t *sf_swz, int64_t R, int64_t C, uint8_t *sf_l
 /* ------------------------------------------------------------- transform -- */
 /* y = x * blockdiag(T, T, ...) for `rows` rows of K values (bs divides K),
  * T a bs x bs bf16 matrix, row-major T[i*bs + j], 1/sqrt(bs) already folded in
- * ([P2] HadamardTransform snippet).  R-xform: fp32 fused multiply-add chain
- * in index order, then one bf16 rounding ([P2] `.to(value.dtype)`).
- * Output y is [rows, K] bf16 with row stride K. */
+ * ([P2] HadamardTransform snippet).  R-xform: y[j] is the exact value of
+ * sum_i x[i]*T[i][j], rounded once to bf16, nearest-even ([P2] `.to(value.dtype)`
+ * of the product).  Output y is [rows, K] bf16 with row stride K.
+ *
+ * The exact sum: a bf16 value is an integer significand of at most 8 bits
+ * times 2^e (e >= -133), so each product is a signed integer of at most 16
+ * bits times 2^(ex+et) with ex+et >= -266.  The products are added as
+ * integers into a fixed-point accumulator whose bit 0 weighs 2^-XF_LSB, held
+ * in 32-bit digits of int64 limbs (each limb absorbs the carries of up to 2^15
+ * additions of 48-bit values before the final normalisation). */
+#define XF_LSB 300
+#define XF_LIMBS 20                     /* bits of weight 2^-300 .. 2^339 */
+
+static void bf16_split(uint16_t h, int64_t *sig, int *e2)
+{
+    const int e = (h >> 7) & 0xFF;
+    int64_t m = h & 0x7F;
+    assert(e != 0xFF);                  /* finite inputs only */
+    if (e != 0) { m |= 0x80; *e2 = e - 134; } else { *e2 = -133; }   /* value = m * 2^e2 */
+    *sig = (h & 0x8000) ? -m : m;
+}
+
+static void acc_normalise(int64_t *limb)
+{
+    for (int i = 0; i + 1 < XF_LIMBS; ++i) {
+        const int64_t low = limb[i] & 0xFFFFFFFFLL;
+        limb[i + 1] += (limb[i] - low) / 4294967296LL;   /* exact: a multiple of 2^32 */
+        limb[i] = low;
+    }
+}
+
+/* bit b (0-based, weight 2^(b - XF_LSB)) of a normalised non-negative accumulator */
+static int acc_bit(const int64_t *limb, int b)
+{
+    if (b < 0) return 0;
+    return (int)((limb[b / 32] >> (b % 32)) & 1);
+}
+
+/* Round the exact accumulator to bf16, nearest-even. */
+static uint16_t acc_to_bf16(int64_t *limb)
+{
+    acc_normalise(limb);
+    uint16_t sign = 0;
+    if (limb[XF_LIMBS - 1] < 0) {       /* negative: take the magnitude */
+        for (int i = 0; i < XF_LIMBS; ++i) limb[i] = -limb[i];
+        acc_normalise(limb);
+        sign = 0x8000;
+    }
+    int top = -1;                       /* highest set bit */
+    for (int i = XF_LIMBS - 1; i >= 0 && top < 0; --i)
+        for (int b = 31; b >= 0; --b)
+            if ((limb[i] >> b) & 1) { top = i * 32 + b; break; }
+    if (top < 0) return 0;              /* an exact zero sum is +0 */
+    int exp2 = top - XF_LSB;            /* value in [2^exp2, 2^(exp2+1)) */
+    assert(exp2 <= 127);                /* no overflow of the bf16 range in this use */
+    /* keep 8 significant bits, or fewer in the subnormal range (lsb >= 2^-133) */
+    int lsb = top - 7;
+    if (lsb - XF_LSB < -133) lsb = XF_LSB - 133;
+    uint32_t keep = 0;
+    for (int b = top; b >= lsb; --b) keep = (keep << 1) | (uint32_t)acc_bit(limb, b);
+    const int half = acc_bit(limb, lsb - 1);
+    int sticky = 0;
+    for (int b = lsb - 2; b >= 0 && !sticky; --b) sticky = acc_bit(limb, b);
+    if (half && (sticky || (keep & 1))) ++keep;
+    /* value = keep * 2^(lsb - XF_LSB); re-encode (keep may have carried to 2^8 or 2^(n+1)) */
+    int e = lsb - XF_LSB;
+    while (keep >= 0x100) { keep >>= 1; ++e; }      /* only a rounding carry: the dropped bit is 0 */
+    uint16_t out;
+    if (keep >= 0x80) {                 /* normal: keep = 1.m * 2^7 */
+        const int biased = e + 7 + 127;
+        assert(biased >= 1 && biased <= 254);
+        out = (uint16_t)((biased << 7) | (keep & 0x7F));
+    } else {                            /* subnormal: e == -133 */
+        assert(e == -133);
+        out = (uint16_t)keep;
+    }
+    return sign | out;
+}
+
 void oracle_transform_rows(const uint16_t *x, int64_t rows, int64_t K, int64_t ld,
                            const uint16_t *T, int bs, uint16_t *y)
 {
-    assert(bs > 0 && K % bs == 0);
+    assert(bs > 0 && bs <= 32768 && K % bs == 0);
     for (int64_t r = 0; r < rows; ++r)
         for (int64_t g = 0; g < K / bs; ++g)
             for (int j = 0; j < bs; ++j) {
-                float acc = 0.0f;
+                int64_t limb[XF_LIMBS] = {0};
                 for (int i = 0; i < bs; ++i) {
-                    float xi = oracle_bf16_to_f32(x[r * ld + g * bs + i]);
-                    float tij = oracle_bf16_to_f32(T[(int64_t)i * bs + j]);
-                    acc = fmaf(xi, tij, acc);
+                    int64_t sx, st;
+                    int ex, et;
+                    bf16_split(x[r * ld + g * bs + i], &sx, &ex);
+                    bf16_split(T[(int64_t)i * bs + j], &st, &et);
+                    const int64_t p = sx * st;                 /* |p| < 2^16 */
+                    if (p == 0) continue;
+                    const int pos = ex + et + XF_LSB;          /* >= 34 */
+                    assert(pos >= 0 && pos / 32 + 1 < XF_LIMBS);
+                    const int64_t v = p * ((int64_t)1 << (pos % 32));   /* |v| < 2^47 */
+                    limb[pos / 32] += v;
                 }
-                y[r * K + g * bs + j] = oracle_f32_to_bf16(acc);
+                y[r * K + g * bs + j] = acc_to_bf16(limb);
             }
 }
 

@@ -85,6 +85,19 @@ def test_quant_validation(lib):
     assert "overlaps" in nv.nvfp4_last_error_string()
 
 
+def test_quant_export_y_validation(lib):
+    T = A + (1 << 30)
+    Y = A + (1 << 31)
+    f = lambda m=16, t=T, bs=16, y=Y: lib.nvfp4_quant_act_export_y(A, m, 256, 256, B, t, bs, C, D, y, None)
+    assert f(m=0) == OK
+    assert f(t=None, bs=0) == INVALID                        # only with a transform
+    assert f(y=None) == INVALID
+    assert f(y=Y + 8) == ALIGN
+    assert f(y=A + 512) == ALIAS                             # y inside x
+    assert f(y=C) == ALIAS                                   # y over the packed output
+    assert f(bs=24) == INVALID
+
+
 def test_prepare_weight_validation(lib):
     assert lib.nvfp4_prepare_weight(A, 0, 64, 64, B, C, D, None) == OK
     assert lib.nvfp4_prepare_weight(None, 128, 64, 64, B, C, D, None) == INVALID

@@ -1,12 +1,14 @@
 """GPU parity of the quantizers (nvfp4_quant_act, nvfp4_prepare_weight) against
 the CPU oracle: packed FP4 bytes and tiled scale bytes, padding included, must
-match bit for bit."""
+match bit for bit.  With the block-diagonal transform, the codes must match the
+oracle's quantization of the kernel's own bf16 y bit for bit, and y must match
+the exact x * blockdiag(T) within the fp32 accumulation bound."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from _helpers import dev_scalar, gather_scales, nv, require_library, sample_indices, syn
+from _helpers import dev_scalar, gather_scales, nv, require_library, sample_indices, syn, tile_edges
 
 pytestmark = pytest.mark.gpu
 
@@ -135,27 +137,95 @@ def test_prepare_weight_bit_exact():
     _assert_bytes_equal(gather_scales(got[1], rows, sf_lin.shape[1], 4104), sf_lin, "weight scale rows")
 
 
+def _gpu_quant_export(x: torch.Tensor, k: int, gs: float, t: torch.Tensor, bs: int):
+    """The transform quantizer through nvfp4_quant_act_export_y: (packed, tiled
+    scales, y bits); also checks that nvfp4_quant_act writes the same bytes."""
+    m = x.shape[0]
+    xd = x.cuda()
+    fp4 = torch.full((m, nv.padded_k(k) // 2), 0xAB, dtype=torch.uint8, device="cuda")
+    sf = torch.full((nv.nvfp4_scale_bytes(m, k),), 0xCD, dtype=torch.uint8, device="cuda")
+    y = torch.full((m, k), -1, dtype=torch.int16, device="cuda")          # 0xFFFF: a NaN pattern
+    g, td = dev_scalar(gs), t.cuda()
+    nv.nvfp4_quant_act_export_y(xd, m, k, xd.stride(0), g, td, bs, fp4, sf, y)
+    plain = _gpu_quant(x, k, gs, t=t, bs=bs)
+    torch.cuda.synchronize()
+    got = fp4.cpu().numpy(), sf.cpu().numpy(), y.cpu().numpy().view(np.uint16)
+    _assert_bytes_equal(plain[0], got[0], "packed (plain vs export entry point)")
+    _assert_bytes_equal(plain[1], got[1], "scales (plain vs export entry point)")
+    return got
+
+
+def _check_transform_y(y_bits, x: torch.Tensor, t: torch.Tensor, bs: int, rows=None):
+    """The kernel's y against x * blockdiag(T): within half a bf16 step plus the
+    fp32 accumulation bound bs * 2^-23 * sum|x_i T_ij| of the exact sum
+    (float64 matmul of the bf16 values), and equal to the oracle's exactly
+    rounded sum except at a small fraction of near ties.  Returns the number
+    of elements that differ from the oracle's y."""
+    xs = x if rows is None else x[rows]
+    ref = oracle.transform(syn.bf16_bits(xs), syn.bf16_bits(t), bs)
+    xd = xs.double().numpy().reshape(-1, bs)
+    td = t.double().numpy()
+    exact = (xd @ td).reshape(ref.shape)
+    mag = (np.abs(xd) @ np.abs(td)).reshape(ref.shape)
+    yg = (y_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    assert np.isfinite(yg).all(), "y has unwritten elements"
+    half_ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(exact), 2.0 ** -126))) - 8)
+    err = np.abs(yg - exact)
+    tol = half_ulp * 1.0001 + bs * 2.0 ** -23 * mag
+    assert (err <= tol).all(), f"y off by {float((err / tol).max()):.2f} x tolerance"
+    n_diff = int((y_bits != ref).sum())
+    assert n_diff <= max(2, 1e-3 * ref.size), f"{n_diff} of {ref.size} y values differ from the exact rounding"
+    return n_diff
+
+
 @pytest.mark.parametrize("bs", [16, 32, 64, 128])
 @pytest.mark.parametrize("m", [16, 97])
-def test_transform_quant_bit_exact(bs, m):
+def test_transform_quant_parity(bs, m):
+    """Transform + quantizer (reading A12, tiered): y within the fp32
+    accumulation bound of the exact x * blockdiag(T); codes and scales are the
+    oracle's quantization of that y, bit for bit; end to end, against the
+    oracle's exactly rounded y, at most a 1e-4 fraction of bytes differ."""
     p = syn.Problem("transform", f"bs{bs}", m, 4096, 4096, seed=3100 + bs + m, x_kind="student_t", bs=bs)
     x = syn.make_activation(p)
     t = syn.random_hadamard_transform(bs, seed=p.seed)
     gs = float(np.float32(syn.E4M3_MAX * syn.FP4_MAX) / np.float32(syn.transformed_amax(x, t)))
-    got = _gpu_quant(x, 4096, gs, t=t, bs=bs)
+    got_pk, got_sf, y = _gpu_quant_export(x, 4096, gs, t, bs)
+    packed, sf_lin = oracle.quantize(y, gs, k=4096)
+    _assert_bytes_equal(got_pk, packed, f"packed vs oracle(y) bs={bs}")
+    _assert_bytes_equal(got_sf, oracle.swizzle(sf_lin), f"scales vs oracle(y) bs={bs}")
+    _check_transform_y(y, x, t, bs)
     ref = _oracle_quant(x, 4096, gs, t=t, bs=bs)
-    _assert_bytes_equal(got[0], ref[0], f"packed bs={bs}")
-    _assert_bytes_equal(got[1], ref[1], f"scales bs={bs}")
+    n_bad = int((got_pk != ref[0]).sum() + (got_sf != ref[1]).sum())
+    assert n_bad <= max(2, 1e-4 * (got_pk.size + got_sf.size)), f"{n_bad} bytes differ end to end"
+
+
+@pytest.mark.parametrize("bs", [16, 32, 64, 128])
+def test_transform_quant_full_size_sampled(bs):
+    """The transform workload's M = 4096, K = 4096 at full size (32 x 32 tiles
+    of 128 x 128 over the persistent CTAs); sampled rows, tile edges included,
+    checked as in test_transform_quant_parity."""
+    p = [q for q in syn.transform_fused() if q.m == 4096 and q.bs == bs][0]
+    L = syn.make_layer(p)
+    got_pk, got_sf, y = _gpu_quant_export(L.x, p.k, L.gs_x, L.t, bs)
+    rows = sample_indices(p.m, 48, seed=bs, must=tile_edges(p.m, 128))
+    packed, sf_lin = oracle.quantize(y[rows], L.gs_x, k=p.k)
+    _assert_bytes_equal(got_pk[rows], packed, f"packed rows vs oracle(y) bs={bs}")
+    _assert_bytes_equal(gather_scales(got_sf, rows, sf_lin.shape[1], p.k), sf_lin, f"scale rows bs={bs}")
+    # the tiled buffer holds exactly these scales plus zero padding (rows are all < m here)
+    full = oracle.unswizzle(got_sf, p.m, sf_lin.shape[1])
+    assert np.array_equal(oracle.swizzle(full), got_sf)
+    _check_transform_y(y[rows], L.x, L.t, bs, rows=rows)
 
 
 def test_transform_quant_odd_k():
     """k = 4112 (multiple of 16, not of 32): the last scale block is K padding."""
     x = syn.bf16_student_t(40, 4112, 3, seed=75)
     t = syn.random_hadamard_transform(16, seed=75)
-    got = _gpu_quant(x, 4112, 3.0, t=t, bs=16)
-    ref = _oracle_quant(x, 4112, 3.0, t=t, bs=16)
-    _assert_bytes_equal(got[0], ref[0], "packed")
-    _assert_bytes_equal(got[1], ref[1], "scales")
+    got_pk, got_sf, y = _gpu_quant_export(x, 4112, 3.0, t, 16)
+    packed, sf_lin = oracle.quantize(y, 3.0, k=4112)
+    _assert_bytes_equal(got_pk, packed, "packed")
+    _assert_bytes_equal(got_sf, oracle.swizzle(sf_lin), "scales")
+    _check_transform_y(y, x, t, 16)
 
 
 @pytest.mark.parametrize("m,k", [(65536, 16384), (8192, 4096)])

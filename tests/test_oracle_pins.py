@@ -12,6 +12,8 @@ import fractions
 import math
 import os
 
+from fractions import Fraction
+
 import numpy as np
 import pytest
 import torch
@@ -357,20 +359,60 @@ def test_transform_pm1_inputs_give_exact_hadamard_sums(oracle_mod):
     assert np.array_equal(yf.astype(np.float64), exact)
 
 
+def _bf16_rne_exact(q: Fraction) -> float:
+    """Nearest-even bf16 value of an exact rational (8 significant bits; the
+    subnormal quantum is 2^-133)."""
+    if q == 0:
+        return 0.0
+    sign = -1.0 if q < 0 else 1.0
+    a = abs(q)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    assert Fraction(2) ** e <= a < Fraction(2) ** (e + 1)
+    quantum = Fraction(2) ** (max(e, -126) - 7)
+    n = a / quantum
+    fl = n.numerator // n.denominator
+    rem = n - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    return sign * float(fl * quantum)
+
+
 @pytest.mark.parametrize("bs", [16, 32, 64, 128])
-def test_transform_within_fp32_accumulation_bound(oracle_mod, bs):
-    """|y - x*T| <= half a bf16 ulp of the result plus the fp32 accumulation
-    bound bs * 2^-24 * sum|x_i T_ij| (float64 matmul as the library reference)."""
-    x = syn.bf16_student_t(16, 256, 3, seed=18 + bs)
+def test_transform_is_the_exactly_rounded_sum(oracle_mod, bs):
+    """y = bf16_rne(exact sum_i x_i T_ij), checked with rational arithmetic on
+    a small sample (brute force, no floating-point sums)."""
+    x = syn.bf16_student_t(3, 128, 3, seed=18 + bs)
     t = syn.random_hadamard_transform(bs, seed=19 + bs)
     y = oracle_mod.transform(syn.bf16_bits(x), syn.bf16_bits(t), bs)
     yf = (y.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-    xd = x.double().numpy().reshape(-1, bs)
-    td = t.double().numpy()
-    ref = (xd @ td).reshape(16, 256)
-    mag = (np.abs(xd) @ np.abs(td)).reshape(16, 256)
-    half_ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - 8)
-    assert (np.abs(yf - ref) <= half_ulp * 1.0001 + bs * 2.0 ** -24 * mag).all()
+    xq = [[Fraction(float(v)) for v in row] for row in x.float().numpy()]
+    tq = [[Fraction(float(v)) for v in row] for row in t.float().numpy()]
+    for r in range(3):
+        for g in range(128 // bs):
+            for j in range(bs):
+                exact = sum(xq[r][g * bs + i] * tq[i][j] for i in range(bs))
+                assert yf[r, g * bs + j] == _bf16_rne_exact(exact), (r, g, j)
+
+
+def test_transform_rounds_the_exact_sum_not_a_running_fp32_sum(oracle_mod):
+    """(1 + 2^-8 + 2^-30) / 4 lies just above the bf16 midpoint 1/4 + 2^-10, so
+    it rounds up to 1/4 + 2^-9; an fp32 running sum would lose the 2^-32 term,
+    land on the midpoint and round to even (1/4)."""
+    bs = 16
+    t = np.full((bs, bs), 0.25, np.float32)
+    x = np.zeros((1, bs), np.float32)
+    x[0, :4] = [1.0, 2.0 ** -9, 2.0 ** -9, 2.0 ** -30]
+    y = oracle_mod.transform(_bits(x), syn.bf16_bits(torch.from_numpy(t).to(torch.bfloat16)), bs)
+    assert oracle_mod.bf16_to_f32(int(y[0, 0])) == 0.25 + 2.0 ** -9
+    # exact cancellation gives +0; subnormal results keep their exact value
+    x[0, :4] = [1.0, -1.0, 2.0 ** -126, 0.0]
+    t2 = np.eye(bs, dtype=np.float32)
+    t2[:2, 0] = 1.0
+    y = oracle_mod.transform(_bits(x), syn.bf16_bits(torch.from_numpy(t2).to(torch.bfloat16)), bs)
+    assert y[0, 0] == 0x0000
+    assert oracle_mod.bf16_to_f32(int(y[0, 2])) == 2.0 ** -126
 
 
 # ------------------------------------------------------------------ GEMM ----
