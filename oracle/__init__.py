@@ -69,6 +69,10 @@ def _load():
     lib.oracle_unswizzle.argtypes = [P, I64, I64, P]
     lib.oracle_transform_rows.restype = None
     lib.oracle_transform_rows.argtypes = [P, I64, I64, I64, P, ctypes.c_int, P]
+    lib.oracle_act_global_scale.restype = ctypes.c_float
+    lib.oracle_act_global_scale.argtypes = [P, I64, I64, I64]
+    lib.oracle_alpha.restype = ctypes.c_float
+    lib.oracle_alpha.argtypes = [ctypes.c_float, ctypes.c_float]
     lib.oracle_gemm.restype = None
     lib.oracle_gemm.argtypes = [P, P, P, P, I64, P, I64, P, I64, ctypes.c_float, P, P]
     _lib = lib
@@ -187,6 +191,25 @@ def transform(x_bits: np.ndarray, t_bits: np.ndarray, bs: int, k: int | None = N
     if rows:
         lib.oracle_transform_rows(_ptr(x_bits), rows, k, ld, _ptr(t_bits), bs, _ptr(y))
     return y
+
+
+def act_global_scale(x_bits: np.ndarray, t_bits: np.ndarray | None = None, bs: int = 0,
+                     k: int | None = None) -> float:
+    """Dynamic activation global scale fl32(448*6 / amax) over the tensor, of
+    y = bf16(x * blockdiag(T)) when a transform is given (reading R-dyn)."""
+    lib = _load()
+    x_bits = _c(x_bits, np.uint16)
+    rows, ld = x_bits.shape
+    k = ld if k is None else k
+    if t_bits is not None:
+        x_bits = transform(x_bits, t_bits, bs, k)
+        ld = k
+    return float(lib.oracle_act_global_scale(_ptr(x_bits), rows, k, ld))
+
+
+def alpha(gs_x: float, gs_w: float) -> float:
+    """fl32(1 / fl32(gs_x * gs_w))."""
+    return float(_load().oracle_alpha(gs_x, gs_w))
 
 
 def gemm(a_packed, a_sf_lin, b_packed, b_sf_lin, alpha: float, bias_bits=None,

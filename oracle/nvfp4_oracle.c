@@ -34,6 +34,8 @@
  *            rows padded to 128 and columns to 4 with zero bytes.
  *   R-xform  y[j] = bf16_rne(sum_i x[i]*T[i][j]) of the exact sum (no
  *            intermediate rounding; an exact zero sum gives +0).
+ *   R-dyn    dynamic activation scale: gs = fl32(448*6 / amax|v|) over the whole
+ *            tensor (of y with a transform), FLT_MAX on overflow, 1 if amax = 0.
  *   R-gemm   out[m,n] = alpha * sum_k deq(A)[m,k]*deq(B)[n,k] + bias[n] in FP64,
  *            where deq(q) = e2m1(q) * e4m3(sf) (the global scales live in alpha).
  *
@@ -42,6 +44,7 @@
  * so that no multiply-add is fused behind our back.
  */
 #include <assert.h>
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -325,6 +328,35 @@ void oracle_transform_rows(const uint16_t *x, int64_t rows, int64_t K, int64_t l
                 }
                 y[r * K + g * bs + j] = acc_to_bf16(limb);
             }
+}
+
+/* ------------------------------------------------- dynamic global scale -- */
+/* Per-tensor activation scale computed from the data instead of calibrated
+ * ([P2] the AbsMax statistic of fusedQuantizeNv; [P1] input_global_scale_inv
+ * multiplies into the block scale, R-scale).  R-dyn:
+ *   amax = max |v| over the rows x K bf16 values v (the transformed y when a
+ *          transform applies: the caller passes y);
+ *   gs   = fl32(448 * 6 / amax), the largest finite binary32 if that
+ *          overflows, and 1 when amax == 0 (every block scale is 0 then). */
+float oracle_act_global_scale(const uint16_t *x, int64_t rows, int64_t K, int64_t ld)
+{
+    float amax = 0.0f;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t k = 0; k < K; ++k) {
+            const float a = fabsf(oracle_bf16_to_f32(x[r * ld + k]));
+            assert(isfinite(a));
+            if (a > amax) amax = a;
+        }
+    if (amax == 0.0f) return 1.0f;
+    const float gs = 2688.0f / amax;        /* 448 * 6, exact in binary32 */
+    return isinf(gs) ? FLT_MAX : gs;
+}
+
+/* alpha = fl32(1 / fl32(gs_x * gs_w)): the GEMM output scale of [P1]. */
+float oracle_alpha(float gs_x, float gs_w)
+{
+    const float prod = gs_x * gs_w;
+    return 1.0f / prod;
 }
 
 /* ------------------------------------------------------------------ GEMM -- */

@@ -415,6 +415,63 @@ def test_transform_rounds_the_exact_sum_not_a_running_fp32_sum(oracle_mod):
     assert oracle_mod.bf16_to_f32(int(y[0, 2])) == 2.0 ** -126
 
 
+# ------------------------------------------------- dynamic global scale ----
+
+def test_dynamic_scale_closed_forms(oracle_mod):
+    """gs = 448*6/amax: amax 448 -> 6, 2688 -> 1, 1 -> 2688, 0.75 -> 3584; the
+    sign of the extreme element does not matter; an all-zero tensor gives 1;
+    a scale that overflows binary32 is clamped to its largest finite value."""
+    def gs_of(vals):
+        return oracle_mod.act_global_scale(_bits(np.array(vals, np.float32).reshape(1, -1)))
+    assert gs_of([1.0, -448.0, 3.0, 0.0]) == 6.0
+    assert gs_of([2688.0, 5.0]) == 1.0
+    assert gs_of([0.5, -1.0]) == 2688.0
+    assert gs_of([0.75, 0.5]) == 3584.0
+    assert gs_of([0.0, -0.0, 0.0]) == 1.0
+    tiny = np.zeros((1, 8), np.uint16)
+    tiny[0, 3] = 0x0001                                      # smallest bf16 subnormal, 2^-133
+    assert oracle_mod.act_global_scale(tiny) == float(np.finfo(np.float32).max)
+
+
+def test_dynamic_scale_matches_the_calibration_constant(oracle_mod):
+    """The oracle's per-tensor pass equals the host calibration of the input
+    generators (an independent numpy computation of fl32(2688 / amax))."""
+    for seed, (m, k) in enumerate([(7, 256), (64, 4104), (3, 16)]):
+        x = syn.bf16_student_t(m, k, 3, seed=40 + seed)
+        assert oracle_mod.act_global_scale(syn.bf16_bits(x)) == syn.global_scale(x)
+
+
+def test_dynamic_scale_under_transforms_that_keep_magnitudes(oracle_mod):
+    """The identity and a signed permutation leave max |y| = max |x|, so the
+    transformed scale equals the plain one; a Hadamard block changes it."""
+    bs = 16
+    x = syn.bf16_student_t(5, 64, 3, seed=44)
+    xb = syn.bf16_bits(x)
+    plain = oracle_mod.act_global_scale(xb)
+    eye = syn.bf16_bits(torch.eye(bs).to(torch.bfloat16))
+    assert oracle_mod.act_global_scale(xb, eye, bs) == plain
+    rng = np.random.default_rng(45)
+    t = np.zeros((bs, bs), np.float32)
+    t[rng.permutation(bs), np.arange(bs)] = rng.choice([-1.0, 1.0], bs)
+    assert oracle_mod.act_global_scale(xb, syn.bf16_bits(torch.from_numpy(t).to(torch.bfloat16)), bs) == plain
+    h = syn.bf16_bits(syn.random_hadamard_transform(bs, seed=46))
+    assert oracle_mod.act_global_scale(xb, h, bs) != plain
+
+
+def test_dynamic_scale_puts_the_max_block_on_448(oracle_mod):
+    x = syn.bf16_normal((16, 512), 1.0, seed=47)
+    xb = syn.bf16_bits(x)
+    gs = oracle_mod.act_global_scale(xb)
+    _, sf = oracle_mod.quantize(xb, gs)
+    assert sf.max() == 0x7E
+
+
+def test_alpha_closed_forms(oracle_mod):
+    assert oracle_mod.alpha(2.0, 4.0) == 0.125
+    assert oracle_mod.alpha(6.0, 1.0) == float(np.float32(1.0) / np.float32(6.0))
+    assert oracle_mod.alpha(3.0, 0.5) == float(np.float32(2.0) / np.float32(3.0))
+
+
 # ------------------------------------------------------------------ GEMM ----
 
 def _quantized_operands(oracle_mod, m, n, k, seed):
