@@ -591,6 +591,42 @@ def run_suite(args, dev):
         del L, w_fp4, w_sf, ws, a_fp4, a_sf, out
         torch.cuda.empty_cache()
 
+    # the transform quantizer at sizes far above L2 (steady state), and the
+    # dynamic global scale: its amax pass alone and followed by the quantizer
+    for m, bs in [(16384, 16), (16384, 128), (65536, 16), (65536, 128)]:
+        x = syn.bf16_normal((m, 4096), 1.0, 4600 + bs, device=dev)
+        t = syn.random_hadamard_transform(bs, seed=bs).to(dev)
+        gs = torch.tensor([30.0], **f32)
+        x_fp4, x_sf = nv.quant_act(x, gs, t, bs)
+        tq = timed(lambda: nv.nvfp4_quant_act(x, m, 4096, 4096, gs, t, bs, x_fp4, x_sf, stream))
+        nv.nvfp4_device_error()
+        qb = quant_bytes(m, 4096)
+        yield {"suite": "transform_sweep", "m": m, "k": 4096, "bs": bs, "quant_us": round(tq * 1e6, 2),
+               "quant_gbs": round(qb / tq / 1e9, 1), "quant_frac_hbm": round(qb / tq / 1e9 / hbm, 4)}
+        del x, x_fp4, x_sf
+        torch.cuda.empty_cache()
+    for m, k, bs in [(8192, 4096, 0), (8192, 14336, 0), (65536, 16384, 0), (4096, 4096, 128), (65536, 4096, 128)]:
+        x = syn.bf16_normal((m, k), 1.0, 4700 + m % 1000 + bs, device=dev)
+        t = syn.random_hadamard_transform(bs, seed=bs).to(dev) if bs else None
+        gs = torch.empty(1, **f32)
+        x_fp4, x_sf = nv.quant_act(x, torch.tensor([30.0], **f32), t, bs)
+
+        def amax_pass():
+            nv.nvfp4_act_global_scale(x, m, k, k, t, bs, None, gs, None, stream)
+
+        def dynamic_quant():
+            amax_pass()
+            nv.nvfp4_quant_act(x, m, k, k, gs, t, bs, x_fp4, x_sf, stream)
+
+        ta, td = timed(amax_pass), timed(dynamic_quant)
+        nv.nvfp4_device_error()
+        yield {"suite": "global_scale", "m": m, "k": k, "bs": bs, "amax_us": round(ta * 1e6, 2),
+               "amax_read_gbs": round(2 * m * k / ta / 1e9, 1), "amax_frac_hbm": round(2 * m * k / ta / 1e9 / hbm, 4),
+               "dynamic_quant_us": round(td * 1e6, 2),
+               "note": "amax pass (read of x, memset and finalize launches included), then the quantizer"}
+        del x, x_fp4, x_sf
+        torch.cuda.empty_cache()
+
     for m, k, seed in syn.quant_sweep():
         x = syn.bf16_normal((m, k), 1.0, seed, device=dev)
         gs = torch.tensor([syn.global_scale(x)], **f32)

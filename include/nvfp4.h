@@ -161,6 +161,28 @@ nvfp4_status nvfp4_quant_act_export_y(const void *x_bf16, int64_t m, int64_t k, 
                                       uint8_t *x_fp4, uint8_t *x_sf, void *y_bf16,
                                       nvfp4_stream_t stream);
 
+/* Dynamic activation global scale: the per-tensor AbsMax statistic of the
+ * transform page's fusedQuantizeNv computed on the device, for activations
+ * without a calibrated scale (the torch-backend page's input_global_scale_inv
+ * then comes from the data):
+ *   amax         = max |v| over the m x k activation, v = x, or with a
+ *                  transform the bf16 y = x * blockdiag(T) exactly as
+ *                  nvfp4_quant_act computes it (same kernel pipeline);
+ *   gs_out[0]    = fl32(448 * 6 / amax); the largest finite float if that
+ *                  overflows; 1 when amax == 0 (m == 0 included);
+ *   alpha_out[0] = fl32(1 / fl32(gs_out[0] * w_gs_dev[0])) when alpha_out and
+ *                  w_gs_dev are given (both or neither).
+ *   x_bf16, k, ldx, transform_bf16, bs   as for nvfp4_quant_act
+ *   gs_out      out  device fp32; also the pass's scratch word (it holds the
+ *                    amax bits until the last kernel of the call)
+ * gs_out and alpha_out feed nvfp4_quant_act / nvfp4_linear directly; nothing
+ * leaves the device and nothing synchronises, so the sequence can be captured
+ * in a CUDA graph.  Costs one read of x (2 bytes per element) before the
+ * quantizer's; a tensor smaller than L2 is then re-read from L2. */
+nvfp4_status nvfp4_act_global_scale(const void *x_bf16, int64_t m, int64_t k, int64_t ldx,
+                                    const void *transform_bf16, int bs, const float *w_gs_dev,
+                                    float *gs_out, float *alpha_out, nvfp4_stream_t stream);
+
 /* Block-scaled FP4 GEMM with the fused epilogue (torch-backend page:
  * torch._scaled_mm, then * alpha, slice_nvfp4_output, + bias):
  *   out[i, j] = bf16( alpha * sum_k deq(A)[i,k] * deq(W)[j,k] + bias[j] ),

@@ -22,8 +22,8 @@ __all__ = [
     "NVFP4_OK", "Nvfp4Error", "library_path", "load_library", "build",
     "nvfp4_abi_version", "nvfp4_is_supported", "nvfp4_last_error_string", "nvfp4_device_error",
     "nvfp4_packed_bytes", "nvfp4_scale_bytes", "nvfp4_linear_workspace_bytes",
-    "nvfp4_prepare_weight", "nvfp4_quant_act", "nvfp4_quant_act_export_y", "nvfp4_gemm", "nvfp4_linear", "nvfp4_linear_noalloc",
-    "padded_k", "scale_shape",
+    "nvfp4_prepare_weight", "nvfp4_quant_act", "nvfp4_quant_act_export_y", "nvfp4_act_global_scale", "nvfp4_gemm", "nvfp4_linear", "nvfp4_linear_noalloc",
+    "padded_k", "scale_shape", "quant_act", "prepare_weight", "linear", "act_global_scale",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -49,6 +49,7 @@ EXPORTS = [
     ("nvfp4_prepare_weight", _I32, [_P, _I64, _I64, _I64, _P, _P, _P, _P]),
     ("nvfp4_quant_act", _I32, [_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _P]),
     ("nvfp4_quant_act_export_y", _I32, [_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _P, _P]),
+    ("nvfp4_act_global_scale", _I32, [_P, _I64, _I64, _I64, _P, _I32, _P, _P, _P, _P]),
     ("nvfp4_gemm", _I32, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _P, _P, _I64, _P]),
     ("nvfp4_linear", _I32, [_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _I64, _I64, _P, _P, _P, _I64,
                             _P, _SZ, _P]),
@@ -179,6 +180,12 @@ def nvfp4_quant_act_export_y(x, m: int, k: int, ldx: int, gs, transform, bs: int
                                                    _ptr(x_sf), _ptr(y), _stream(stream)))
 
 
+def nvfp4_act_global_scale(x, m: int, k: int, ldx: int, transform, bs: int, w_gs, gs_out, alpha_out,
+                           stream=None) -> None:
+    _check(load_library().nvfp4_act_global_scale(_ptr(x), m, k, ldx, _ptr(transform), bs, _ptr(w_gs),
+                                                 _ptr(gs_out), _ptr(alpha_out), _stream(stream)))
+
+
 def nvfp4_gemm(a_fp4, a_sf, m: int, w_fp4, w_sf, n_w: int, n_out: int, k: int, alpha, bias, out, ldo: int,
                stream=None) -> None:
     _check(load_library().nvfp4_gemm(_ptr(a_fp4), _ptr(a_sf), m, _ptr(w_fp4), _ptr(w_sf), n_w, n_out, k,
@@ -214,6 +221,18 @@ def quant_act(x, gs, transform=None, bs: int = 0, stream=None):
     x_sf = torch.empty(max(nvfp4_scale_bytes(m, k), 1), dtype=torch.uint8, device=x.device)
     nvfp4_quant_act(x, m, k, _ld(x, "x"), gs, transform, bs if transform is not None else 0, x_fp4, x_sf, stream)
     return x_fp4, x_sf
+
+
+def act_global_scale(x, transform=None, bs: int = 0, w_gs=None, stream=None):
+    """Dynamic scale of a [m, k] bf16 CUDA tensor; returns (gs, alpha) as
+    1-element fp32 device tensors (alpha is None without w_gs)."""
+    import torch
+    m, k = x.shape
+    gs = torch.empty(1, dtype=torch.float32, device=x.device)
+    alpha = torch.empty(1, dtype=torch.float32, device=x.device) if w_gs is not None else None
+    nvfp4_act_global_scale(x, m, k, _ld(x, "x"), transform, bs if transform is not None else 0, w_gs, gs, alpha,
+                           stream)
+    return gs, alpha
 
 
 def prepare_weight(w, w_gs, stream=None):

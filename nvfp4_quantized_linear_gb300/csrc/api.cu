@@ -173,6 +173,7 @@ nvfp4::QuantParams quant_params(const void *x, int64_t m, int64_t k, int64_t ldx
     p.bs = t ? bs : 0;
     p.err_flag = nullptr;
     p.y_out = nullptr;
+    p.amax_out = nullptr;
     return p;
 }
 
@@ -448,6 +449,36 @@ nvfp4_status nvfp4_quant_act_export_y(const void *x_bf16, int64_t m, int64_t k, 
     nvfp4::QuantParams p = quant_params(x_bf16, m, k, ldx, gs_dev, transform_bf16, bs, x_fp4, x_sf);
     p.y_out = static_cast<uint16_t *>(y_bf16);
     return run_quant(p, num_sms, reinterpret_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status nvfp4_act_global_scale(const void *x_bf16, int64_t m, int64_t k, int64_t ldx, const void *transform_bf16,
+                                    int bs, const float *w_gs_dev, float *gs_out, float *alpha_out, nvfp4_stream_t stream)
+{
+    // the quantizer's checks, with gs_out standing in for the (absent) outputs' alignment
+    if (!gs_out) return fail(NVFP4_ERR_INVALID_ARG, "null pointer argument");
+    if ((alpha_out != nullptr) != (w_gs_dev != nullptr))
+        return fail(NVFP4_ERR_INVALID_ARG, "alpha_out and w_gs_dev go together");
+    if ((reinterpret_cast<uintptr_t>(gs_out) & 3) || (reinterpret_cast<uintptr_t>(alpha_out) & 3) ||
+        (reinterpret_cast<uintptr_t>(w_gs_dev) & 3))
+        return fail(NVFP4_ERR_ALIGNMENT, "scalars must be 4-byte aligned");
+    const uint8_t *dummy = reinterpret_cast<const uint8_t *>(16);
+    nvfp4_status st = check_quant_args(m > 0 ? x_bf16 : nullptr, m, k, ldx, gs_out, transform_bf16, bs, dummy, dummy,
+                                       "x");
+    if (st != NVFP4_OK) return st;
+    Range outs[2] = {range(gs_out, 4, "gs_out"), range(alpha_out, alpha_out ? 4 : 0, "alpha_out")};
+    Range ins[3] = {range2d(m > 0 ? x_bf16 : nullptr, m, k, ldx, "x"), range(w_gs_dev, w_gs_dev ? 4 : 0, "w_gs"),
+                    range(transform_bf16, transform_bf16 ? (size_t)bs * bs * 2 : 0, "transform")};
+    if ((st = check_aliases(outs, 2, ins, 3)) != NVFP4_OK) return st;
+    int num_sms = 0;
+    if ((st = current_device(&num_sms)) != NVFP4_OK) return st;
+    nvfp4::QuantParams p = quant_params(x_bf16, m, k, ldx, nullptr, transform_bf16, bs, nullptr, nullptr);
+    cudaError_t e = nvfp4::device_error_word(&p.err_flag);
+    if (e != cudaSuccess) return launch_status(e, "global-scale pass (error word)");
+    const char *why = nullptr;
+    e = nvfp4::launch_act_global_scale(p, w_gs_dev, gs_out, alpha_out, num_sms, reinterpret_cast<cudaStream_t>(stream),
+                                       &why);
+    if (why) return fail(NVFP4_ERR_CUDA, "%s", why);
+    return launch_status(e, "global-scale pass");
 }
 
 nvfp4_status nvfp4_prepare_weight(const void *w_bf16, int64_t n, int64_t k, int64_t ldw, const float *w_gs_dev,

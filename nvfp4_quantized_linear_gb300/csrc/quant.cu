@@ -167,6 +167,57 @@ __global__ void __launch_bounds__(256) quant_kernel(const QuantParams p)
 }
 
 // ---------------------------------------------------------------------------
+// Per-tensor amax of the activation (no transform): the task split of
+// quant_kernel (512-element row segments, U per warp loaded before use), an
+// integer max over the bf16 magnitudes (the bits without the sign order like
+// the values), one atomic max per warp.  Loads keep the default L2 policy so
+// that a tensor smaller than L2 is still there for the quantizer.
+template <int U>
+__global__ void __launch_bounds__(256) act_amax_kernel(const QuantParams p)
+{
+    const int lane = threadIdx.x & 31;
+    const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int nwarps = (int)((gridDim.x * blockDim.x) >> 5);
+    const int segs = (p.k + 511) >> 9;
+    const int tasks = p.m * segs;                     // < 2^31: checked on the host
+    uint32_t mx = 0;                                  // two 16-bit maxima
+    for (int base = warp * U; base < tasks; base += nwarps * U) {
+        Raw16 raw[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int t = base + u;
+            const int r = t / segs;
+            const bool ok = t < tasks;
+            raw[u] = load16(ok ? p.x + (int64_t)r * p.ldx : p.x, (t - r * segs) * 512 + lane * 16, p.k, ok);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint32_t w[8] = {raw[u].a.x, raw[u].a.y, raw[u].a.z, raw[u].a.w,
+                                   raw[u].b.x, raw[u].b.y, raw[u].b.z, raw[u].b.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx = __vmaxu2(mx, w[i] & 0x7FFF7FFFu);
+        }
+    }
+    const uint32_t v = __reduce_max_sync(~0u, max(mx & 0xFFFFu, mx >> 16));
+    if (lane == 0 && v != 0) atomicMax(p.amax_out, v);
+}
+
+// gs = fl32(448 * 6 / amax) from the bf16 bits left in *word by the amax
+// pass, written over it; FLT_MAX if the quotient overflows, 1 for amax == 0.
+// With w_gs: alpha = fl32(1 / fl32(gs * w_gs)).
+__global__ void act_scale_finalize_kernel(unsigned int *word, const float *w_gs, float *alpha)
+{
+    const float amax = __uint_as_float(*word << 16);
+    float gs = 1.0f;
+    if (amax > 0.0f) {
+        gs = __fdiv_rn(2688.0f, amax);
+        if (isinf(gs)) gs = 3.402823466e38f;
+    }
+    *reinterpret_cast<float *>(word) = gs;
+    if (alpha != nullptr) *alpha = __fdiv_rn(1.0f, __fmul_rn(gs, *w_gs));
+}
+
+// ---------------------------------------------------------------------------
 // Transform + quantizer on the tensor cores.  y = x * blockdiag(T) is a dense
 // contraction per bs-block, so each 128-row x 128-column tile of x goes
 // through tcgen05.mma (kind::f16: bf16 operands, fp32 accumulation in TMEM):
@@ -210,6 +261,9 @@ static_assert(kXfSmemBytes <= 232448, "shared memory budget");
 
 __device__ __forceinline__ float round_bf16(float f) { return __bfloat162float(__float2bfloat16_rn(f)); }
 
+// kAmaxOnly: the same pipeline computes y and only reduces max |y| over the
+// tensor into *p.amax_out (no codes, scales or y written).
+template <bool kAmaxOnly>
 __global__ void __launch_bounds__(kXfThreads, 1)
     quant_transform_kernel(const __grid_constant__ CUtensorMap tmX, const QuantParams p)
 {
@@ -274,8 +328,8 @@ __global__ void __launch_bounds__(kXfThreads, 1)
         }
     }
     fence_proxy_async_shared();                   // the MMAs read T^T through the async proxy
-    const float gs = __ldg(p.gs);
-    fill_inv_table(inv_tab, gs);
+    const float gs = kAmaxOnly ? 1.0f : __ldg(p.gs);   // the amax pass has no scale yet
+    if (!kAmaxOnly) fill_inv_table(inv_tab, gs);
     if (warp == 1) {
         tmem_alloc(tmem_slot, kXfTmemCols);
         tmem_relinquish();
@@ -293,6 +347,7 @@ __global__ void __launch_bounds__(kXfThreads, 1)
         const int q = warp & 3;
         const int h = (warp - kXfEpiWarp0) >> 2;
         const int64_t out_ld = p.kp >> 1;
+        float tmax = 0.0f;                                // kAmaxOnly: this thread's max |y|
         int it = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
             const int b = it & 1;
@@ -327,6 +382,10 @@ __global__ void __launch_bounds__(kXfThreads, 1)
                     y1[j] = round_bf16(__uint_as_float(a[8 + j]));
                     amax = fmaxf(amax, fmaxf(fabsf(y0[j]), fabsf(y1[j])));
                 }
+                if constexpr (kAmaxOnly) {
+                    tmax = fmaxf(tmax, amax);
+                    continue;
+                }
                 float inv;
                 const uint32_t sf = block_scale_tab(amax, gs, inv_tab, inv);
                 pk[2 * u] = quant8(y0, inv);
@@ -344,6 +403,7 @@ __global__ void __launch_bounds__(kXfThreads, 1)
                     dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
                 }
             }
+            if constexpr (kAmaxOnly) continue;
             if (r < p.m) {
                 uint8_t *o = p.out + r * out_ld + (c0 >> 1);
 #pragma unroll
@@ -360,10 +420,17 @@ __global__ void __launch_bounds__(kXfThreads, 1)
                     *reinterpret_cast<uint16_t *>(p.sf + sf_offset(r, cs, p.nbp)) = (uint16_t)sfw;
             }
         }
+        if constexpr (kAmaxOnly) {
+            // max |y| is a bf16 value (a max of bf16 values): its top 16 bits
+            // order like the magnitudes, so an integer max over bits is exact
+            const uint32_t v = __reduce_max_sync(~0u, __float_as_uint(tmax) >> 16);
+            if (lane == 0 && v != 0) atomicMax(p.amax_out, v);
+        }
     } else if (warp == 0) {
         if (lane == 0) {
             // --------------------------------------------------------- producer --
-            const uint64_t pol = l2_policy_evict_first();   // x is read once
+            // x is read once; the amax pass leaves it in L2 for the quantizer that follows
+            const uint64_t pol = kAmaxOnly ? l2_policy_evict_normal() : l2_policy_evict_first();
             int it = 0;
             for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
                 const int stage = it % kXfStages;
@@ -445,14 +512,19 @@ cudaError_t launch_quant(const QuantParams &p, int num_sms, cudaStream_t s)
     return cudaGetLastError();
 }
 
-cudaError_t launch_quant_transform(const QuantParams &p, int num_sms, cudaStream_t s, const char **why)
+namespace {
+
+// Sets the shared-memory attribute of both transform-kernel variants (once
+// per device), encodes the activation's tensor map and launches one variant.
+template <bool kAmaxOnly>
+cudaError_t launch_transform_variant(const QuantParams &p, int num_sms, cudaStream_t s, const char **why)
 {
     static int configured_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(quant_transform_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kXfSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(quant_transform_kernel<kAmaxOnly>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kXfSmemBytes);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
@@ -464,7 +536,40 @@ cudaError_t launch_quant_transform(const QuantParams &p, int num_sms, cudaStream
     const int64_t n_ct = ((int64_t)p.nbp * 16 + kXfCols - 1) / kXfCols;
     const int64_t tiles = (int64_t)(p.mp / kXfRows) * n_ct;
     const int grid = (int)(tiles < num_sms ? tiles : num_sms);
-    quant_transform_kernel<<<(unsigned)grid, kXfThreads, kXfSmemBytes, s>>>(tmX, p);
+    quant_transform_kernel<kAmaxOnly><<<(unsigned)grid, kXfThreads, kXfSmemBytes, s>>>(tmX, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_quant_transform(const QuantParams &p, int num_sms, cudaStream_t s, const char **why)
+{
+    return launch_transform_variant<false>(p, num_sms, s, why);
+}
+
+cudaError_t launch_act_global_scale(QuantParams p, const float *w_gs, float *gs_out, float *alpha_out, int num_sms,
+                                    cudaStream_t s, const char **why)
+{
+    unsigned int *word = reinterpret_cast<unsigned int *>(gs_out);
+    cudaError_t e = cudaMemsetAsync(word, 0, sizeof(unsigned int), s);
+    if (e != cudaSuccess) return e;
+    p.amax_out = word;
+    if (p.m > 0) {
+        if (p.bs) {
+            e = launch_transform_variant<true>(p, num_sms, s, why);
+        } else {
+            constexpr int U = 4;
+            const int64_t tasks = (int64_t)p.m * ((p.k + 511) / 512);
+            int64_t blocks = ((tasks + U - 1) / U + 7) / 8;
+            const int64_t cap = (int64_t)num_sms * 8;
+            if (blocks > cap) blocks = cap;
+            if (blocks < 1) blocks = 1;
+            act_amax_kernel<U><<<(unsigned)blocks, 256, 0, s>>>(p);
+            e = cudaGetLastError();
+        }
+        if (e != cudaSuccess) return e;
+    }
+    act_scale_finalize_kernel<<<1, 1, 0, s>>>(word, alpha_out != nullptr ? w_gs : nullptr, alpha_out);
     return cudaGetLastError();
 }
 

@@ -276,9 +276,11 @@ static uint16_t acc_to_bf16(int64_t *limb)
         sign = 0x8000;
     }
     int top = -1;                       /* highest set bit */
-    for (int i = XF_LIMBS - 1; i >= 0 && top < 0; --i)
+    int hi = XF_LIMBS - 1;
+    while (hi >= 0 && limb[hi] == 0) --hi;
+    if (hi >= 0)
         for (int b = 31; b >= 0; --b)
-            if ((limb[i] >> b) & 1) { top = i * 32 + b; break; }
+            if ((limb[hi] >> b) & 1) { top = hi * 32 + b; break; }
     if (top < 0) return 0;              /* an exact zero sum is +0 */
     int exp2 = top - XF_LSB;            /* value in [2^exp2, 2^(exp2+1)) */
     assert(exp2 <= 127);                /* no overflow of the bf16 range in this use */
@@ -288,8 +290,14 @@ static uint16_t acc_to_bf16(int64_t *limb)
     uint32_t keep = 0;
     for (int b = top; b >= lsb; --b) keep = (keep << 1) | (uint32_t)acc_bit(limb, b);
     const int half = acc_bit(limb, lsb - 1);
-    int sticky = 0;
-    for (int b = lsb - 2; b >= 0 && !sticky; --b) sticky = acc_bit(limb, b);
+    int sticky = 0;                     /* any set bit in [0, lsb - 2] */
+    const int sb = lsb - 2;
+    if (sb >= 0) {
+        const int q = sb / 32, r = sb % 32;
+        const int64_t mask = (r == 31) ? (int64_t)0xFFFFFFFF : (((int64_t)1 << (r + 1)) - 1);
+        sticky = (limb[q] & mask) != 0;
+        for (int i = q - 1; i >= 0 && !sticky; --i) sticky = limb[i] != 0;
+    }
     if (half && (sticky || (keep & 1))) ++keep;
     /* value = keep * 2^(lsb - XF_LSB); re-encode (keep may have carried to 2^8 or 2^(n+1)) */
     int e = lsb - XF_LSB;

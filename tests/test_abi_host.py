@@ -98,6 +98,23 @@ def test_quant_export_y_validation(lib):
     assert f(bs=24) == INVALID
 
 
+def test_act_global_scale_validation(lib):
+    G, AL, WG = C, C + 64, D
+    f = lambda x=A, m=16, k=256, ldx=256, t=None, bs=0, wg=None, gs=G, al=None: \
+        lib.nvfp4_act_global_scale(x, m, k, ldx, t, bs, wg, gs, al, None)
+    assert f(gs=None) == INVALID
+    assert f(wg=WG) == INVALID                               # w_gs without alpha_out
+    assert f(al=AL) == INVALID                               # alpha_out without w_gs
+    assert f(gs=G + 2) == ALIGN
+    assert f(x=None) == INVALID
+    assert f(ldx=100) == INVALID
+    assert f(x=A + 8) == ALIGN
+    assert f(t=A + B, bs=24) == INVALID
+    assert f(gs=A + 64) == ALIAS                             # scale output inside x
+    assert f(wg=WG, al=WG) == ALIAS                          # alpha over w_gs
+    assert f(wg=WG, al=G) == ALIAS                           # alpha over gs
+
+
 def test_prepare_weight_validation(lib):
     assert lib.nvfp4_prepare_weight(A, 0, 64, 64, B, C, D, None) == OK
     assert lib.nvfp4_prepare_weight(None, 128, 64, 64, B, C, D, None) == INVALID
