@@ -69,6 +69,12 @@ def _load():
     lib.oracle_unswizzle.argtypes = [P, I64, I64, P]
     lib.oracle_transform_rows.restype = None
     lib.oracle_transform_rows.argtypes = [P, I64, I64, I64, P, ctypes.c_int, P]
+    lib.oracle_mx_scale_code.restype = ctypes.c_uint8
+    lib.oracle_mx_scale_code.argtypes = [ctypes.c_float]
+    lib.oracle_dec_e8m0.restype = ctypes.c_double
+    lib.oracle_dec_e8m0.argtypes = [ctypes.c_uint8]
+    lib.oracle_quantize_rows_mx.restype = None
+    lib.oracle_quantize_rows_mx.argtypes = [P, I64, I64, I64, P, P]
     lib.oracle_act_global_scale.restype = ctypes.c_float
     lib.oracle_act_global_scale.argtypes = [P, I64, I64, I64]
     lib.oracle_alpha.restype = ctypes.c_float
@@ -152,6 +158,31 @@ def quantize(x_bits: np.ndarray, gs: float, k: int | None = None):
     sf = np.zeros((rows, kp // 16), np.uint8)
     if rows:
         lib.oracle_quantize_rows(_ptr(x_bits), rows, k, ld, ctypes.c_float(gs), _ptr(packed), _ptr(sf))
+    return packed, sf
+
+
+def mx_scale_code(amax: float) -> int:
+    """E8M0 code of an MXFP4 block with absolute maximum amax (reading R-mx)."""
+    return int(_load().oracle_mx_scale_code(amax))
+
+
+def dec_e8m0(code: int) -> float:
+    return _load().oracle_dec_e8m0(code)
+
+
+def quantize_mx(x_bits: np.ndarray, k: int | None = None):
+    """Quantize bf16 rows to MXFP4 (page "B12X", the MXFP4 linear backend's
+    dynamic activation quantization; OCP MX v1.0 format, reading R-mx).
+    Returns (packed [rows, Kp/2] uint8, sf_lin [rows, Kp/32] uint8 E8M0 codes)."""
+    lib = _load()
+    x_bits = _c(x_bits, np.uint16)
+    rows, ld = x_bits.shape
+    k = ld if k is None else k
+    kp = padded_k(k)
+    packed = np.zeros((rows, kp // 2), np.uint8)
+    sf = np.zeros((rows, kp // 32), np.uint8)
+    if rows:
+        lib.oracle_quantize_rows_mx(_ptr(x_bits), rows, k, ld, _ptr(packed), _ptr(sf))
     return packed, sf
 
 

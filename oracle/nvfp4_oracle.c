@@ -36,6 +36,8 @@
  *            intermediate rounding; an exact zero sum gives +0).
  *   R-dyn    dynamic activation scale: gs = fl32(448*6 / amax|v|) over the whole
  *            tensor (of y with a transform), FLT_MAX on overflow, 1 if amax = 0.
+ *   R-mx     MXFP4: blocks of 32, E8M0 scale 2^s with s = clamp(floor(log2 amax) - 2,
+ *            -127, 127) (-127 for a zero block), q = e2m1(fl32(v * 2^-s)), no global scale.
  *   R-gemm   out[m,n] = alpha * sum_k deq(A)[m,k]*deq(B)[n,k] + bias[n] in FP64,
  *            where deq(q) = e2m1(q) * e4m3(sf) (the global scales live in alpha).
  *
@@ -190,6 +192,72 @@ void oracle_quantize_rows(const uint16_t *x, int64_t rows, int64_t K, int64_t ld
                 float p0 = v[i] * inv, p1 = v[i + 1] * inv;
                 uint8_t q0 = oracle_enc_e2m1(p0), q1 = oracle_enc_e2m1(p1);
                 packed[r * (Kp / 2) + (b * 16 + i) / 2] = (uint8_t)(q0 | (q1 << 4));
+            }
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ MXFP4 -- */
+/* MXFP4 (the B12X page's MXFP4 linear backend, dynamic activations; format of
+ * the OCP Microscaling (MX) v1.0 specification): blocks of 32 E2M1 elements
+ * sharing one E8M0 scale X = 2^s, code s + 127 (no sign; 0xFF is NaN), and
+ * no per-tensor scale.  R-mx:
+ *   s   = clamp(floor(log2(amax)) - 2, -127, 127), 2 being the exponent of the
+ *         largest E2M1 value (6 = 1.5 * 2^2); an all-zero block gets s = -127;
+ *   q_i = e2m1_rne_satfinite(fl32(v_i * 2^-s))   (|v_i| up to 7.99 * 2^s
+ *         saturates to 6 * 2^s, as the specification's conversion does).     */
+static int floor_log2_pos(float a)          /* a > 0, finite */
+{
+    const uint32_t u = bits_from_f32(a);
+    const int e = (int)((u >> 23) & 0xFF);
+    if (e != 0) return e - 127;
+    uint32_t f = u & 0x7FFFFFu;
+    int top = 22;
+    while (!((f >> top) & 1u)) --top;
+    return -149 + top;                      /* binary32 subnormal */
+}
+
+uint8_t oracle_mx_scale_code(float amax)
+{
+    assert(isfinite(amax) && amax >= 0.0f);
+    if (amax == 0.0f) return 0;
+    int s = floor_log2_pos(amax) - 2;
+    if (s < -127) s = -127;
+    if (s > 127) s = 127;
+    return (uint8_t)(s + 127);
+}
+
+double oracle_dec_e8m0(uint8_t code)
+{
+    assert(code != 0xFF && "oracle: E8M0 NaN code");
+    return ldexp(1.0, (int)code - 127);
+}
+
+/* Quantize `rows` rows of K bf16 values to MXFP4; K is zero-extended to
+ * Kp = roundup(K, 32) (R-pad).  packed [rows, Kp/2] as for NVFP4 (R-nibble);
+ * sf_lin [rows, Kp/32] E8M0 codes, row-major (unswizzled). */
+void oracle_quantize_rows_mx(const uint16_t *x, int64_t rows, int64_t K, int64_t ld, uint8_t *packed,
+                             uint8_t *sf_lin)
+{
+    const int64_t Kp = (K + 31) / 32 * 32, nb = Kp / 32;
+    for (int64_t r = 0; r < rows; ++r) {
+        const uint16_t *xr = x + r * ld;
+        for (int64_t b = 0; b < nb; ++b) {
+            float v[32];
+            float amax = 0.0f;
+            for (int i = 0; i < 32; ++i) {
+                const int64_t k = b * 32 + i;
+                v[i] = (k < K) ? oracle_bf16_to_f32(xr[k]) : 0.0f;
+                const float a = fabsf(v[i]);
+                if (a > amax) amax = a;
+            }
+            const uint8_t code = oracle_mx_scale_code(amax);
+            const float mul = (float)ldexp(1.0, 127 - (int)code);     /* 2^-s: exact in binary32 */
+            sf_lin[r * nb + b] = code;
+            for (int i = 0; i < 32; i += 2) {
+                const float p0 = v[i] * mul, p1 = v[i + 1] * mul;
+                packed[r * (Kp / 2) + (b * 32 + i) / 2] =
+                    (uint8_t)(oracle_enc_e2m1(p0) | (oracle_enc_e2m1(p1) << 4));
             }
         }
     }

@@ -415,6 +415,77 @@ def test_transform_rounds_the_exact_sum_not_a_running_fp32_sum(oracle_mod):
     assert oracle_mod.bf16_to_f32(int(y[0, 2])) == 2.0 ** -126
 
 
+# ------------------------------------------------------------------- MXFP4 ----
+
+def test_e8m0_decode_closed_forms(oracle_mod):
+    assert oracle_mod.dec_e8m0(127) == 1.0
+    assert oracle_mod.dec_e8m0(0) == 2.0 ** -127
+    assert oracle_mod.dec_e8m0(254) == 2.0 ** 127
+    assert oracle_mod.dec_e8m0(130) == 8.0
+
+
+def test_mx_scale_rule(oracle_mod):
+    """s = floor(log2 amax) - 2: amax in [4, 8) -> 2^0 (code 127), [8, 16) -> 2^1,
+    [0.5, 1) -> 2^-3; clamped to [-127, 127]; zero block -> code 0."""
+    code = oracle_mod.mx_scale_code
+    assert code(4.0) == code(6.0) == code(7.99) == 127
+    assert code(8.0) == 128 and code(0.75) == 124
+    assert code(0.0) == 0
+    assert code(2.0 ** -140) == 0                                   # clamped at s = -127
+    assert code(float(np.finfo(np.float32).max)) == 127 + 125       # floor(log2) = 127 -> s = 125
+    for e in range(-120, 120, 7):                                    # every power of two: s = e - 2
+        assert code(2.0 ** e) == e - 2 + 127
+
+
+def test_mx_exact_roundtrip_of_representable_blocks(oracle_mod):
+    """Blocks of 32 E2M1 grid values times 2^e with 6 * 2^e present: the scale is
+    2^e and every element comes back exactly."""
+    rng = np.random.default_rng(50)
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6], np.float64)
+    for e in (-10, -3, 0, 2, 9):
+        vals = rng.choice(grid, size=(4, 64)) * rng.choice([-1.0, 1.0], size=(4, 64))
+        vals[:, 0] = 6.0
+        vals[:, 32] = -6.0
+        x = vals * 2.0 ** e
+        packed, sf = oracle_mod.quantize_mx(_bits(x))
+        assert (sf == e + 127).all()
+        back = np.array([[oracle_mod.dec_e2m1(int((packed[r, c // 2] >> (4 * (c % 2))) & 0xF)) for c in range(64)]
+                         for r in range(4)])
+        assert np.array_equal(back * 2.0 ** e, x)
+
+
+def test_mx_saturates_between_6_and_8_times_the_scale(oracle_mod):
+    x = np.zeros((1, 32), np.float32)
+    x[0, :3] = [7.5, -7.0, 5.0]                 # amax 7.5 -> s = 0: 7.5 and -7 clamp to +-6, 5 ties to 4
+    packed, sf = oracle_mod.quantize_mx(_bits(x))
+    assert sf[0, 0] == 127
+    assert packed[0, 0] == (0x7 | (0xF << 4)) and (packed[0, 1] & 0xF) == 0x6
+
+
+def test_mx_zero_block_and_padding(oracle_mod):
+    x = syn.bf16_normal((3, 40), 1.0, seed=51).float().numpy()
+    x[1, :32] = 0.0
+    packed, sf = oracle_mod.quantize_mx(_bits(x), k=40)
+    assert packed.shape == (3, 32) and sf.shape == (3, 2)        # Kp = 64: two blocks
+    assert sf[1, 0] == 0 and (packed[1, :16] == 0).all()
+    assert (packed[:, 20:] == 0).all()                           # columns 40..63 are zero padding
+
+
+def test_mx_elements_are_nearest_grid_points(oracle_mod):
+    """Brute force: each element's code decodes to a grid point nearest to
+    v * 2^-s (ties to the even code), with the block's own s."""
+    x = syn.bf16_student_t(4, 128, 3, seed=52)
+    xf = x.float().numpy().astype(np.float64)
+    packed, sf = oracle_mod.quantize_mx(syn.bf16_bits(x))
+    mags = np.array([oracle_mod.dec_e2m1(c) for c in range(8)])
+    for r in range(4):
+        for c in range(128):
+            code = (packed[r, c // 2] >> (4 * (c % 2))) & 0xF
+            t = abs(xf[r, c]) * 2.0 ** (127 - int(sf[r, c // 32]))
+            d = np.abs(mags - min(t, 6.0))
+            assert d[code & 7] == d.min()
+
+
 # ------------------------------------------------- dynamic global scale ----
 
 def test_dynamic_scale_closed_forms(oracle_mod):
