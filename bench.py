@@ -627,6 +627,18 @@ def run_suite(args, dev):
         del x, x_fp4, x_sf
         torch.cuda.empty_cache()
 
+    # MXFP4 activation quantization (block 32, E8M0 scales, no global scale)
+    for m, k in [(8192, 4096), (8192, 14336), (65536, 16384)]:
+        x = syn.bf16_normal((m, k), 1.0, 4800 + m % 1000, device=dev)
+        x_fp4, x_sf = nv.quant_act_mx(x)
+        tq = timed(lambda: nv.nvfp4_mxfp4_quant_act(x, m, k, k, x_fp4, x_sf, stream))
+        nv.nvfp4_device_error()
+        qb = 2 * m * k + m * nv.padded_k(k) // 2 + nv.nvfp4_mxfp4_scale_bytes(m, k)
+        yield {"suite": "mxfp4_quant", "m": m, "k": k, "quant_us": round(tq * 1e6, 2),
+               "quant_gbs": round(qb / tq / 1e9, 1), "quant_frac_hbm": round(qb / tq / 1e9 / hbm, 4), "bytes": qb}
+        del x, x_fp4, x_sf
+        torch.cuda.empty_cache()
+
     for m, k, seed in syn.quant_sweep():
         x = syn.bf16_normal((m, k), 1.0, seed, device=dev)
         gs = torch.tensor([syn.global_scale(x)], **f32)

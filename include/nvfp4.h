@@ -161,6 +161,22 @@ nvfp4_status nvfp4_quant_act_export_y(const void *x_bf16, int64_t m, int64_t k, 
                                       uint8_t *x_fp4, uint8_t *x_sf, void *y_bf16,
                                       nvfp4_stream_t stream);
 
+/* MXFP4 activation quantization, the format of the B12X page's MXFP4 linear
+ * backend (dynamic activations; OCP Microscaling v1.0): 32-element blocks of
+ * E2M1 values sharing one E8M0 scale 2^s, no per-tensor scale:
+ *   s    = clamp(floor(log2(amax)) - 2, -127, 127), -127 for an all-zero block;
+ *   code = s + 127 (one byte per block);  q_i = e2m1_rne_satfinite(v_i * 2^-s).
+ *   x_bf16  in   [m, ldx] bf16, the first k columns are the data
+ *   x_fp4   out  nvfp4_packed_bytes(m, k) bytes: K padded to roundup(k,32) with
+ *                zeros, two codes per byte, the even element in the low nibble
+ *   x_sf    out  nvfp4_mxfp4_scale_bytes(m, k) bytes: the scale codes in the
+ *                tiled layout of the NVFP4 scales (512-byte tiles of 128 rows x
+ *                4 columns), one column per 32 elements, zero padding
+ * Validation, aliasing and error behaviour as for nvfp4_quant_act. */
+size_t nvfp4_mxfp4_scale_bytes(int64_t rows, int64_t k);   /* roundup(rows,128) * roundup(roundup(k,32)/32, 4) */
+nvfp4_status nvfp4_mxfp4_quant_act(const void *x_bf16, int64_t m, int64_t k, int64_t ldx,
+                                   uint8_t *x_fp4, uint8_t *x_sf, nvfp4_stream_t stream);
+
 /* Dynamic activation global scale: the per-tensor AbsMax statistic of the
  * transform page's fusedQuantizeNv computed on the device, for activations
  * without a calibrated scale (the torch-backend page's input_global_scale_inv

@@ -22,8 +22,9 @@ __all__ = [
     "NVFP4_OK", "Nvfp4Error", "library_path", "load_library", "build",
     "nvfp4_abi_version", "nvfp4_is_supported", "nvfp4_last_error_string", "nvfp4_device_error",
     "nvfp4_packed_bytes", "nvfp4_scale_bytes", "nvfp4_linear_workspace_bytes",
-    "nvfp4_prepare_weight", "nvfp4_quant_act", "nvfp4_quant_act_export_y", "nvfp4_act_global_scale", "nvfp4_gemm", "nvfp4_linear", "nvfp4_linear_noalloc",
-    "padded_k", "scale_shape", "quant_act", "prepare_weight", "linear", "act_global_scale",
+    "nvfp4_prepare_weight", "nvfp4_quant_act", "nvfp4_quant_act_export_y", "nvfp4_act_global_scale", "nvfp4_mxfp4_scale_bytes", "nvfp4_mxfp4_quant_act",
+    "nvfp4_gemm", "nvfp4_linear", "nvfp4_linear_noalloc",
+    "padded_k", "scale_shape", "quant_act", "quant_act_mx", "prepare_weight", "linear", "act_global_scale",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -50,6 +51,8 @@ EXPORTS = [
     ("nvfp4_quant_act", _I32, [_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _P]),
     ("nvfp4_quant_act_export_y", _I32, [_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _P, _P]),
     ("nvfp4_act_global_scale", _I32, [_P, _I64, _I64, _I64, _P, _I32, _P, _P, _P, _P]),
+    ("nvfp4_mxfp4_scale_bytes", _SZ, [_I64, _I64]),
+    ("nvfp4_mxfp4_quant_act", _I32, [_P, _I64, _I64, _I64, _P, _P, _P]),
     ("nvfp4_gemm", _I32, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _P, _P, _I64, _P]),
     ("nvfp4_linear", _I32, [_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _I64, _I64, _P, _P, _P, _I64,
                             _P, _SZ, _P]),
@@ -186,6 +189,14 @@ def nvfp4_act_global_scale(x, m: int, k: int, ldx: int, transform, bs: int, w_gs
                                                  _ptr(gs_out), _ptr(alpha_out), _stream(stream)))
 
 
+def nvfp4_mxfp4_scale_bytes(rows: int, k: int) -> int:
+    return load_library().nvfp4_mxfp4_scale_bytes(rows, k)
+
+
+def nvfp4_mxfp4_quant_act(x, m: int, k: int, ldx: int, x_fp4, x_sf, stream=None) -> None:
+    _check(load_library().nvfp4_mxfp4_quant_act(_ptr(x), m, k, ldx, _ptr(x_fp4), _ptr(x_sf), _stream(stream)))
+
+
 def nvfp4_gemm(a_fp4, a_sf, m: int, w_fp4, w_sf, n_w: int, n_out: int, k: int, alpha, bias, out, ldo: int,
                stream=None) -> None:
     _check(load_library().nvfp4_gemm(_ptr(a_fp4), _ptr(a_sf), m, _ptr(w_fp4), _ptr(w_sf), n_w, n_out, k,
@@ -233,6 +244,16 @@ def act_global_scale(x, transform=None, bs: int = 0, w_gs=None, stream=None):
     nvfp4_act_global_scale(x, m, k, _ld(x, "x"), transform, bs if transform is not None else 0, w_gs, gs, alpha,
                            stream)
     return gs, alpha
+
+
+def quant_act_mx(x, stream=None):
+    """MXFP4-quantize a [m, k] bf16 CUDA tensor; returns (x_fp4 [m, Kp/2], x_sf flat E8M0 codes)."""
+    import torch
+    m, k = x.shape
+    x_fp4 = torch.empty((m, padded_k(k) // 2), dtype=torch.uint8, device=x.device)
+    x_sf = torch.empty(max(nvfp4_mxfp4_scale_bytes(m, k), 1), dtype=torch.uint8, device=x.device)
+    nvfp4_mxfp4_quant_act(x, m, k, _ld(x, "x"), x_fp4, x_sf, stream)
+    return x_fp4, x_sf
 
 
 def prepare_weight(w, w_gs, stream=None):

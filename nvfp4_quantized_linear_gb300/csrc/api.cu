@@ -405,6 +405,12 @@ size_t nvfp4_scale_bytes(int64_t rows, int64_t k)
     return (size_t)nvfp4::rows_padded(rows) * (size_t)nvfp4::scale_cols_padded(k);
 }
 
+size_t nvfp4_mxfp4_scale_bytes(int64_t rows, int64_t k)
+{
+    if (rows <= 0 || k <= 0) return 0;
+    return (size_t)nvfp4::rows_padded(rows) * (size_t)((nvfp4::padded_k(k) / 32 + 3) / 4 * 4);
+}
+
 size_t nvfp4_linear_workspace_bytes(int64_t m, int64_t k, int64_t n_w)
 {
     (void)n_w;
@@ -449,6 +455,26 @@ nvfp4_status nvfp4_quant_act_export_y(const void *x_bf16, int64_t m, int64_t k, 
     nvfp4::QuantParams p = quant_params(x_bf16, m, k, ldx, gs_dev, transform_bf16, bs, x_fp4, x_sf);
     p.y_out = static_cast<uint16_t *>(y_bf16);
     return run_quant(p, num_sms, reinterpret_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status nvfp4_mxfp4_quant_act(const void *x_bf16, int64_t m, int64_t k, int64_t ldx, uint8_t *x_fp4, uint8_t *x_sf,
+                                   nvfp4_stream_t stream)
+{
+    // MXFP4 has no global scale: x_sf stands in for check_quant_args' scale pointer
+    nvfp4_status st = check_quant_args(x_bf16, m, k, ldx, reinterpret_cast<const float *>(x_sf), nullptr, 0, x_fp4,
+                                       x_sf, "x");
+    if (st != NVFP4_OK) return st;
+    if (m == 0) return ok();
+    Range outs[2] = {range(x_fp4, nvfp4_packed_bytes(m, k), "x_fp4"), range(x_sf, nvfp4_mxfp4_scale_bytes(m, k), "x_sf")};
+    Range ins[1] = {range2d(x_bf16, m, k, ldx, "x")};
+    if ((st = check_aliases(outs, 2, ins, 1)) != NVFP4_OK) return st;
+    int num_sms = 0;
+    if ((st = current_device(&num_sms)) != NVFP4_OK) return st;
+    nvfp4::QuantParams p = quant_params(x_bf16, m, k, ldx, nullptr, nullptr, 0, x_fp4, x_sf);
+    p.nb = (int32_t)(nvfp4::padded_k(k) / 32);
+    p.nbp = (p.nb + 3) / 4 * 4;
+    return launch_status(nvfp4::launch_quant_mx(p, num_sms, reinterpret_cast<cudaStream_t>(stream)),
+                         "MXFP4 quantize kernel");
 }
 
 nvfp4_status nvfp4_act_global_scale(const void *x_bf16, int64_t m, int64_t k, int64_t ldx, const void *transform_bf16,

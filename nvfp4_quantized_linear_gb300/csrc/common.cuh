@@ -69,6 +69,8 @@ struct GemmParams {
 // Launchers (return a cudaError_t; no host synchronisation).
 cudaError_t launch_quant(const QuantParams &p, int num_sms, cudaStream_t s);
 cudaError_t launch_quant_transform(const QuantParams &p, int num_sms, cudaStream_t s, const char **why);
+// MXFP4 quantizer: p.nb = kp / 32 scale columns, p.nbp = roundup(nb, 4), no gs.
+cudaError_t launch_quant_mx(const QuantParams &p, int num_sms, cudaStream_t s);
 // Dynamic global scale: max |v| over the activation (of the transformed y when
 // p.bs != 0) into *gs_out as bf16 bits, then gs = fl32(2688 / amax) in place
 // (FLT_MAX on overflow, 1 for amax == 0) and, with w_gs, alpha = 1/(gs * w_gs).

@@ -167,6 +167,80 @@ __global__ void __launch_bounds__(256) quant_kernel(const QuantParams p)
 }
 
 // ---------------------------------------------------------------------------
+// MXFP4 quantizer (OCP MX: 32-element blocks, E8M0 scale 2^s, no global
+// scale).  The task split and loads of quant_kernel; a block is the 32
+// elements of a lane pair, whose maxima meet through one shuffle:
+//     s = clamp(floor(log2 amax) - 2, -127, 127)  (-127 for a zero block),
+//     code = s + 127,  q_i = e2m1(fl32(v_i * 2^-s)).
+// floor(log2 amax) comes from the fp32 bits (exponent field, or the top set
+// bit of a subnormal); 2^-s is built from bits (s <= 125 for finite input).
+// Lanes 0, 8, 16, 24 store the codes of four consecutive blocks as one word
+// of a 512-byte scale tile (the tiled layout of the NVFP4 scales, one column
+// per 32 elements); p.nb / p.nbp count these columns.
+__device__ __forceinline__ uint32_t mx_scale_code(float amax)
+{
+    if (amax == 0.0f) return 0;
+    const uint32_t u = __float_as_uint(amax);
+    const int e = (int)(u >> 23);                       // amax >= 0: no sign bit
+    const int fl = e != 0 ? e - 127 : -149 + (31 - __clz((int)u));
+    const int s = min(max(fl - 2, -127), 127);
+    return (uint32_t)(s + 127);
+}
+
+template <int U>
+__global__ void __launch_bounds__(256) quant_mx_kernel(const QuantParams p)
+{
+    const int lane = threadIdx.x & 31;
+    const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int nwarps = (int)((gridDim.x * blockDim.x) >> 5);
+    if (threadIdx.x == 0) griddep_launch_dependents();
+    const int segs = (p.kp + 511) >> 9;
+    const int tasks = p.mp * segs;                    // < 2^31: checked on the host
+    const int64_t out_ld = p.kp >> 1;
+
+    for (int base = warp * U; base < tasks; base += nwarps * U) {
+        int r0 = base / segs;
+        int s0 = base - r0 * segs;
+        Raw16 raw[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            int r = r0, s = s0 + u;
+            while (s >= segs) { s -= segs; ++r; }
+            const bool row_ok = (base + u < tasks) && (r < p.m);
+            raw[u] = load16(row_ok ? p.x + (int64_t)r * p.ldx : p.x, s * 512 + lane * 16, p.k, row_ok);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (base + u >= tasks) break;                 // uniform across the warp
+            int r = r0, s = s0 + u;
+            while (s >= segs) { s -= segs; ++r; }
+            const int k0 = s * 512 + lane * 16;
+            float v0[8], v1[8];
+            unpack8(raw[u].a, v0);
+            unpack8(raw[u].b, v1);
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(v0[i]), fabsf(v1[i])));
+            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+            const uint32_t code = mx_scale_code(amax);
+            const float mul = __uint_as_float((254u - code) << 23);     // 2^-s, s = code - 127 <= 125
+            if (r < p.m && k0 < p.kp) {
+                uint2 pk;
+                pk.x = quant8(v0, mul);
+                pk.y = quant8(v1, mul);
+                *reinterpret_cast<uint2 *>(p.out + (int64_t)r * out_ld + (k0 >> 1)) = pk;
+            }
+            const uint32_t c1 = __shfl_down_sync(kFull, code, 2);
+            const uint32_t c2 = __shfl_down_sync(kFull, code, 4);
+            const uint32_t c3 = __shfl_down_sync(kFull, code, 6);
+            const int c = s * 16 + (lane >> 1);
+            if ((lane & 7) == 0 && c < p.nb)
+                *reinterpret_cast<uint32_t *>(p.sf + sf_offset(r, c, p.nbp)) = code | (c1 << 8) | (c2 << 16) | (c3 << 24);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Per-tensor amax of the activation (no transform): the task split of
 // quant_kernel (512-element row segments, U per warp loaded before use), an
 // integer max over the bf16 magnitudes (the bits without the sign order like
@@ -545,6 +619,19 @@ cudaError_t launch_transform_variant(const QuantParams &p, int num_sms, cudaStre
 cudaError_t launch_quant_transform(const QuantParams &p, int num_sms, cudaStream_t s, const char **why)
 {
     return launch_transform_variant<false>(p, num_sms, s, why);
+}
+
+cudaError_t launch_quant_mx(const QuantParams &p, int num_sms, cudaStream_t s)
+{
+    constexpr int U = 4;
+    const int64_t segs = (p.kp + 511) / 512;
+    const int64_t tasks = (int64_t)p.mp * segs;
+    int64_t blocks = ((tasks + U - 1) / U + 7) / 8;
+    const int64_t cap = (int64_t)num_sms * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    quant_mx_kernel<U><<<(unsigned)blocks, 256, 0, s>>>(p);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_act_global_scale(QuantParams p, const float *w_gs, float *gs_out, float *alpha_out, int num_sms,

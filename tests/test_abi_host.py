@@ -31,7 +31,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(nvfp4_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(nvfp4_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declarations_are_all_exported(lib):
@@ -113,6 +113,20 @@ def test_act_global_scale_validation(lib):
     assert f(gs=A + 64) == ALIAS                             # scale output inside x
     assert f(wg=WG, al=WG) == ALIAS                          # alpha over w_gs
     assert f(wg=WG, al=G) == ALIAS                           # alpha over gs
+
+
+def test_mxfp4_validation_and_sizes(lib):
+    assert nv.nvfp4_mxfp4_scale_bytes(1, 4096) == 128 * 128          # 128 blocks -> 128 columns
+    assert nv.nvfp4_mxfp4_scale_bytes(129, 4104) == 256 * 132        # Kp 4128 -> 129 blocks -> 132
+    assert nv.nvfp4_mxfp4_scale_bytes(0, 4096) == 0
+    f = lambda x=A, m=16, k=256, ldx=256, out=C, sf=D: lib.nvfp4_mxfp4_quant_act(x, m, k, ldx, out, sf, None)
+    assert f(m=0) == OK
+    assert f(x=None) == INVALID
+    assert f(sf=None) == INVALID
+    assert f(ldx=100) == INVALID
+    assert f(x=A + 8) == ALIGN
+    assert f(out=A + 64) == ALIAS
+    assert f(sf=C + 1024) == ALIAS                         # scales over the packed output (2 KB)
 
 
 def test_prepare_weight_validation(lib):
