@@ -75,6 +75,8 @@ def _load():
     lib.oracle_dec_e8m0.argtypes = [ctypes.c_uint8]
     lib.oracle_quantize_rows_mx.restype = None
     lib.oracle_quantize_rows_mx.argtypes = [P, I64, I64, I64, P, P]
+    lib.oracle_gemm_mx.restype = None
+    lib.oracle_gemm_mx.argtypes = [P, P, P, P, I64, P, I64, P, I64, P, P]
     lib.oracle_act_global_scale.restype = ctypes.c_float
     lib.oracle_act_global_scale.argtypes = [P, I64, I64, I64]
     lib.oracle_alpha.restype = ctypes.c_float
@@ -272,6 +274,30 @@ def gemm(a_packed, a_sf_lin, b_packed, b_sf_lin, alpha: float, bias_bits=None,
         lib.oracle_gemm(_ptr(a_packed), _ptr(a_sf_lin), _ptr(b_packed), _ptr(b_sf_lin), kp,
                         _ptr(rows), rows.size, _ptr(cols), cols.size, ctypes.c_float(alpha),
                         bias_p, _ptr(out))
+    return out
+
+
+def gemm_mx(a_packed, a_sf_lin, b_packed, b_sf_lin, bias_bits=None, rows=None, cols=None) -> np.ndarray:
+    """FP64 reference of an MXFP4 linear (page "B12X", the MXFP4 backend's
+    mm_mxfp4; reading R-mx): sum_k deq(A) deq(B) + bias, E8M0 scales per 32
+    elements, no global scale.  Arguments as for gemm, with [*, Kp/32] scales."""
+    lib = _load()
+    a_packed = _c(a_packed, np.uint8)
+    b_packed = _c(b_packed, np.uint8)
+    a_sf_lin = _c(a_sf_lin, np.uint8)
+    b_sf_lin = _c(b_sf_lin, np.uint8)
+    kp = a_packed.shape[1] * 2
+    assert b_packed.shape[1] * 2 == kp and a_sf_lin.shape[1] == kp // 32 == b_sf_lin.shape[1]
+    rows = _c(np.arange(a_packed.shape[0]) if rows is None else np.asarray(rows), np.int64)
+    cols = _c(np.arange(b_packed.shape[0]) if cols is None else np.asarray(cols), np.int64)
+    out = np.zeros((rows.size, cols.size), np.float64)
+    bias_p = None
+    if bias_bits is not None:
+        bias_keep = _c(bias_bits, np.uint16)          # held until the call returns
+        bias_p = _ptr(bias_keep)
+    if rows.size and cols.size:
+        lib.oracle_gemm_mx(_ptr(a_packed), _ptr(a_sf_lin), _ptr(b_packed), _ptr(b_sf_lin), kp,
+                           _ptr(rows), rows.size, _ptr(cols), cols.size, bias_p, _ptr(out))
     return out
 
 

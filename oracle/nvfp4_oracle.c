@@ -478,3 +478,46 @@ void oracle_gemm(const uint8_t *A, const uint8_t *sfA, const uint8_t *B, const u
     free(a_deq);
     free(b_deq);
 }
+
+/* ------------------------------------------------------------ MXFP4 GEMM -- */
+/* Reference of an MXFP4 linear (R-mx operands): out[i][j] = sum_k
+ * e2m1(A[m,k]) 2^(sfA[m,k/32]-127) e2m1(B[n,k]) 2^(sfB[n,k/32]-127) + bias[n],
+ * FP64, k ascending; m = row_idx[i], n = col_idx[j]; sfA [*, Kp/32] and
+ * sfB [*, Kp/32] linear E8M0 codes; no global scale (MX has none), bias may
+ * be NULL.  Every product is a dyadic rational of at most 4 significant bits
+ * times a power of two, so the FP64 sum is exact whenever the exponent span
+ * of the terms stays within 49 bits. */
+void oracle_gemm_mx(const uint8_t *A, const uint8_t *sfA, const uint8_t *B, const uint8_t *sfB, int64_t Kp,
+                    const int64_t *row_idx, int64_t n_rows, const int64_t *col_idx, int64_t n_cols,
+                    const uint16_t *bias, double *out)
+{
+    const int64_t nb = Kp / 32, kb = Kp / 2;
+    double *a_deq = (double *)malloc(sizeof(double) * (size_t)(Kp * (n_rows > 0 ? n_rows : 1)));
+    double *b_deq = (double *)malloc(sizeof(double) * (size_t)Kp);
+    assert(a_deq && b_deq);
+    for (int64_t i = 0; i < n_rows; ++i) {
+        const int64_t m = row_idx[i];
+        for (int64_t k = 0; k < Kp; ++k) {
+            const uint8_t byte = A[m * kb + k / 2];
+            const uint8_t q = (k & 1) ? (byte >> 4) : (byte & 0xF);
+            a_deq[i * Kp + k] = oracle_dec_e2m1(q) * oracle_dec_e8m0(sfA[m * nb + k / 32]);
+        }
+    }
+    for (int64_t j = 0; j < n_cols; ++j) {
+        const int64_t n = col_idx[j];
+        for (int64_t k = 0; k < Kp; ++k) {
+            const uint8_t byte = B[n * kb + k / 2];
+            const uint8_t q = (k & 1) ? (byte >> 4) : (byte & 0xF);
+            b_deq[k] = oracle_dec_e2m1(q) * oracle_dec_e8m0(sfB[n * nb + k / 32]);
+        }
+        for (int64_t i = 0; i < n_rows; ++i) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < Kp; ++k) acc += a_deq[i * Kp + k] * b_deq[k];
+            if (bias) acc += (double)oracle_bf16_to_f32(bias[n]);
+            out[i * n_cols + j] = acc;
+        }
+    }
+    free(a_deq);
+    free(b_deq);
+}
+

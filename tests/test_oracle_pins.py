@@ -486,6 +486,60 @@ def test_mx_elements_are_nearest_grid_points(oracle_mod):
             assert d[code & 7] == d.min()
 
 
+def _mx_deq_exact(packed, sf, r, k):
+    """Exact rational value of element (r, k) of an MXFP4 operand."""
+    code = int((packed[r, k // 2] >> (4 * (k % 2))) & 0xF)
+    mag = [Fraction(0), Fraction(1, 2), Fraction(1), Fraction(3, 2), Fraction(2), Fraction(3), Fraction(4),
+           Fraction(6)][code & 7]
+    e = int(sf[r, k // 32]) - 127
+    v = mag * (Fraction(2) ** e)
+    return -v if code & 8 else v
+
+
+def test_mx_gemm_matches_exact_rational_brute_force(oracle_mod):
+    """Tiny MXFP4 GEMMs against exact rational sums of the decoded operands
+    (scales spread over 2^-20 .. 2^20), plus a bf16 bias."""
+    rng = np.random.default_rng(55)
+    m, n, k = 5, 7, 96
+    xa = rng.standard_normal((m, k)) * 2.0 ** rng.integers(-20, 20, (m, 1))
+    xb = rng.standard_normal((n, k)) * 2.0 ** rng.integers(-20, 20, (n, 1))
+    a, sa = oracle_mod.quantize_mx(_bits(xa))
+    b, sb = oracle_mod.quantize_mx(_bits(xb))
+    bias = _bits(rng.standard_normal(n))
+    got = oracle_mod.gemm_mx(a, sa, b, sb, bias)
+    for i in range(m):
+        for j in range(n):
+            exact = sum(_mx_deq_exact(a, sa, i, kk) * _mx_deq_exact(b, sb, j, kk) for kk in range(k))
+            exact += Fraction(oracle_mod.bf16_to_f32(int(bias[j])))
+            assert got[i, j] == float(exact), (i, j)
+
+
+def test_mx_gemm_matches_float64_matmul_of_dequantized(oracle_mod):
+    x = syn.bf16_normal((9, 160), 1.0, seed=56)
+    w = syn.bf16_normal((11, 160), 0.02, seed=57)
+    a, sa = oracle_mod.quantize_mx(syn.bf16_bits(x))
+    b, sb = oracle_mod.quantize_mx(syn.bf16_bits(w))
+    def deq(p, s):
+        codes = np.stack([p & 0xF, p >> 4], axis=-1).reshape(p.shape[0], -1)
+        mags = np.array([oracle_mod.dec_e2m1(c) for c in range(16)])[codes]
+        return mags * np.repeat(2.0 ** (s.astype(np.float64) - 127), 32, axis=1)
+    ref = deq(a, sa) @ deq(b, sb).T
+    assert np.allclose(oracle_mod.gemm_mx(a, sa, b, sb), ref, rtol=1e-12, atol=0)
+
+
+def test_mx_gemm_approximates_the_bf16_product(oracle_mod):
+    """Quantization error of MXFP4 on both operands: relative Frobenius error of
+    the product a few percent (E2M1's 3-bit grid, power-of-two scales)."""
+    x = syn.bf16_normal((16, 512), 1.0, seed=58)
+    w = syn.bf16_normal((24, 512), 0.02, seed=59)
+    a, sa = oracle_mod.quantize_mx(syn.bf16_bits(x))
+    b, sb = oracle_mod.quantize_mx(syn.bf16_bits(w))
+    ref = x.double().numpy() @ w.double().numpy().T
+    got = oracle_mod.gemm_mx(a, sa, b, sb)
+    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert 0.02 < rel < 0.25, rel
+
+
 # ------------------------------------------------- dynamic global scale ----
 
 def test_dynamic_scale_closed_forms(oracle_mod):
