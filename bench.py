@@ -46,8 +46,8 @@ FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense FP4 : bf16 tensor rate of G
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 CPU_SAMPLE_ROWS = 16                 # cpu_baseline sample: rows x columns of every linear
 CPU_SAMPLE_COLS = 1024
-REF_STEP_ROWS = 2                    # reference arm: rows per linear per step
-REF_STEP_COLS = 512
+REF_STEP_ROWS = CPU_SAMPLE_ROWS      # reference arm: the cpu_baseline sample, one per step
+REF_STEP_COLS = CPU_SAMPLE_COLS
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "gemm_llama_m8192_traffic.txt")
 
 
