@@ -10,6 +10,7 @@
 #include <string>
 
 #include "common.cuh"
+#include "quant_launch.cuh"
 #include "nvfp4.h"
 
 namespace {
@@ -173,7 +174,6 @@ nvfp4::QuantParams quant_params(const void *x, int64_t m, int64_t k, int64_t ldx
     p.bs = t ? bs : 0;
     p.err_flag = nullptr;
     p.y_out = nullptr;
-    p.amax_out = nullptr;
     return p;
 }
 

@@ -39,7 +39,6 @@ struct QuantParams {
     int32_t bs;
     unsigned int *err_flag;  // device error word (transform kernel's bounded waits)
     uint16_t *y_out;         // nullptr, or [m, k] bf16: the transform result (row stride k)
-    unsigned int *amax_out;  // per-tensor amax pass: bf16 bits of max |v|, atomic max
 };
 
 constexpr int kMaxSplits = 16;       // split-K ranges at most
@@ -69,13 +68,6 @@ struct GemmParams {
 // Launchers (return a cudaError_t; no host synchronisation).
 cudaError_t launch_quant(const QuantParams &p, int num_sms, cudaStream_t s);
 cudaError_t launch_quant_transform(const QuantParams &p, int num_sms, cudaStream_t s, const char **why);
-// MXFP4 quantizer: p.nb = kp / 32 scale columns, p.nbp = roundup(nb, 4), no gs.
-cudaError_t launch_quant_mx(const QuantParams &p, int num_sms, cudaStream_t s);
-// Dynamic global scale: max |v| over the activation (of the transformed y when
-// p.bs != 0) into *gs_out as bf16 bits, then gs = fl32(2688 / amax) in place
-// (FLT_MAX on overflow, 1 for amax == 0) and, with w_gs, alpha = 1/(gs * w_gs).
-cudaError_t launch_act_global_scale(QuantParams p, const float *w_gs, float *gs_out, float *alpha_out, int num_sms,
-                                    cudaStream_t s, const char **why);
 // dependent = true launches the GEMM as a programmatic dependent of the
 // preceding kernel, which must be the quantizer of its activation operand:
 // the GEMM's weight-side loads then start before that kernel has finished.

@@ -16,12 +16,20 @@
 #include "common.cuh"
 #include "gemm_common.cuh"
 #include "ptx.cuh"
+#include "quant_launch.cuh"
 #include "scale_math.cuh"
 
 namespace nvfp4 {
 namespace {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
+
+__device__ __forceinline__ uint64_t l2_policy_evict_normal()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -247,7 +255,7 @@ __global__ void __launch_bounds__(256) quant_mx_kernel(const QuantParams p)
 // the values), one atomic max per warp.  Loads keep the default L2 policy so
 // that a tensor smaller than L2 is still there for the quantizer.
 template <int U>
-__global__ void __launch_bounds__(256) act_amax_kernel(const QuantParams p)
+__global__ void __launch_bounds__(256) act_amax_kernel(const QuantParams p, unsigned int *amax_out)
 {
     const int lane = threadIdx.x & 31;
     const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
@@ -273,7 +281,7 @@ __global__ void __launch_bounds__(256) act_amax_kernel(const QuantParams p)
         }
     }
     const uint32_t v = __reduce_max_sync(~0u, max(mx & 0xFFFFu, mx >> 16));
-    if (lane == 0 && v != 0) atomicMax(p.amax_out, v);
+    if (lane == 0 && v != 0) atomicMax(amax_out, v);
 }
 
 // gs = fl32(448 * 6 / amax) from the bf16 bits left in *word by the amax
@@ -336,10 +344,10 @@ static_assert(kXfSmemBytes <= 232448, "shared memory budget");
 __device__ __forceinline__ float round_bf16(float f) { return __bfloat162float(__float2bfloat16_rn(f)); }
 
 // kAmaxOnly: the same pipeline computes y and only reduces max |y| over the
-// tensor into *p.amax_out (no codes, scales or y written).
+// tensor into *amax_out, as bf16 bits (no codes, scales or y written).
 template <bool kAmaxOnly>
 __global__ void __launch_bounds__(kXfThreads, 1)
-    quant_transform_kernel(const __grid_constant__ CUtensorMap tmX, const QuantParams p)
+    quant_transform_kernel(const __grid_constant__ CUtensorMap tmX, const QuantParams p, unsigned int *amax_out)
 {
     extern __shared__ uint8_t xf_smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(xf_smem_raw) + 1023) & ~uintptr_t(1023));
@@ -498,7 +506,7 @@ __global__ void __launch_bounds__(kXfThreads, 1)
             // max |y| is a bf16 value (a max of bf16 values): its top 16 bits
             // order like the magnitudes, so an integer max over bits is exact
             const uint32_t v = __reduce_max_sync(~0u, __float_as_uint(tmax) >> 16);
-            if (lane == 0 && v != 0) atomicMax(p.amax_out, v);
+            if (lane == 0 && v != 0) atomicMax(amax_out, v);
         }
     } else if (warp == 0) {
         if (lane == 0) {
@@ -591,7 +599,8 @@ namespace {
 // Sets the shared-memory attribute of both transform-kernel variants (once
 // per device), encodes the activation's tensor map and launches one variant.
 template <bool kAmaxOnly>
-cudaError_t launch_transform_variant(const QuantParams &p, int num_sms, cudaStream_t s, const char **why)
+cudaError_t launch_transform_variant(const QuantParams &p, unsigned int *amax_out, int num_sms, cudaStream_t s,
+                                     const char **why)
 {
     static int configured_device = -1;
     int dev = 0;
@@ -610,7 +619,7 @@ cudaError_t launch_transform_variant(const QuantParams &p, int num_sms, cudaStre
     const int64_t n_ct = ((int64_t)p.nbp * 16 + kXfCols - 1) / kXfCols;
     const int64_t tiles = (int64_t)(p.mp / kXfRows) * n_ct;
     const int grid = (int)(tiles < num_sms ? tiles : num_sms);
-    quant_transform_kernel<kAmaxOnly><<<(unsigned)grid, kXfThreads, kXfSmemBytes, s>>>(tmX, p);
+    quant_transform_kernel<kAmaxOnly><<<(unsigned)grid, kXfThreads, kXfSmemBytes, s>>>(tmX, p, amax_out);
     return cudaGetLastError();
 }
 
@@ -618,7 +627,7 @@ cudaError_t launch_transform_variant(const QuantParams &p, int num_sms, cudaStre
 
 cudaError_t launch_quant_transform(const QuantParams &p, int num_sms, cudaStream_t s, const char **why)
 {
-    return launch_transform_variant<false>(p, num_sms, s, why);
+    return launch_transform_variant<false>(p, nullptr, num_sms, s, why);
 }
 
 cudaError_t launch_quant_mx(const QuantParams &p, int num_sms, cudaStream_t s)
@@ -634,16 +643,15 @@ cudaError_t launch_quant_mx(const QuantParams &p, int num_sms, cudaStream_t s)
     return cudaGetLastError();
 }
 
-cudaError_t launch_act_global_scale(QuantParams p, const float *w_gs, float *gs_out, float *alpha_out, int num_sms,
-                                    cudaStream_t s, const char **why)
+cudaError_t launch_act_global_scale(const QuantParams &p, const float *w_gs, float *gs_out, float *alpha_out,
+                                    int num_sms, cudaStream_t s, const char **why)
 {
     unsigned int *word = reinterpret_cast<unsigned int *>(gs_out);
     cudaError_t e = cudaMemsetAsync(word, 0, sizeof(unsigned int), s);
     if (e != cudaSuccess) return e;
-    p.amax_out = word;
     if (p.m > 0) {
         if (p.bs) {
-            e = launch_transform_variant<true>(p, num_sms, s, why);
+            e = launch_transform_variant<true>(p, word, num_sms, s, why);
         } else {
             constexpr int U = 4;
             const int64_t tasks = (int64_t)p.m * ((p.k + 511) / 512);
@@ -651,7 +659,7 @@ cudaError_t launch_act_global_scale(QuantParams p, const float *w_gs, float *gs_
             const int64_t cap = (int64_t)num_sms * 8;
             if (blocks > cap) blocks = cap;
             if (blocks < 1) blocks = 1;
-            act_amax_kernel<U><<<(unsigned)blocks, 256, 0, s>>>(p);
+            act_amax_kernel<U><<<(unsigned)blocks, 256, 0, s>>>(p, word);
             e = cudaGetLastError();
         }
         if (e != cudaSuccess) return e;
