@@ -20,7 +20,12 @@
  *       caller-preallocated outputs that never alias the inputs.
  *   [b12x page]  "B12X quantized linear backends" (vLLM PR #52016), NVFP4
  *       snippet: a non-contiguous 2-D view of the input goes straight into the
- *       quantizer (no contiguous copy); alpha is handed to the GEMM.
+ *       quantizer (no contiguous copy); alpha is handed to the GEMM; packed
+ *       weight storage is reused on reload so captured CUDA graphs stay valid.
+ *       Its MXFP4 backend (dynamic activations) names the second format, whose
+ *       activation quantizer is nvfp4_mxfp4_quant_act.
+ *   Beyond the pages' calibrated scales, nvfp4_act_global_scale computes the
+ *   activation global scale from the data on the device.
  *
  * Number formats.  FP4 = E2M1 (values 0, 0.5, 1, 1.5, 2, 3, 4, 6 and their
  * negatives), two per byte, the even-index element in the low nibble.  Block
@@ -48,10 +53,11 @@
  *   - Outputs may not overlap any input (NVFP4_ERR_ALIAS).
  *   - Row strides are in elements; every base pointer and every row must start
  *     on a 16-byte boundary (NVFP4_ERR_ALIGNMENT).
- *   - m == 0 (or n == 0 for the weight) is a valid empty call: NVFP4_OK, no launch.
+ *   - m == 0 (or n == 0 for the weight) is a valid empty call: NVFP4_OK, no launch
+ *     (nvfp4_act_global_scale still writes its defined result for m == 0).
  *   - Global scales and alpha are read on the device, so no call waits for the
  *     host or synchronises with it.
- *   - A kernel that waits longer than about a second on one of its own
+ *   - A kernel that waits longer than about two seconds on one of its own
  *     pipeline barriers abandons the launch and raises a device error flag
  *     that nvfp4_device_error() reports (NVFP4_ERR_TIMEOUT); it never hangs.
  */
