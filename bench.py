@@ -20,6 +20,12 @@ alpha/bias/bf16 epilogue).  Weights are prepared once, outside the timed region.
   cpu_baseline  the CPU oracle (single thread) on a bounded sample of the same
              workload: sampled rows x sampled output columns of each linear
 
+--suite prints, instead of the headline line, one JSON line per layer problem
+of every workload (Llama / Qwen / padded-K / transform: quantizer, GEMM and
+nvfp4_linear timed alone with a cold L2) and per point of the sweeps
+(quantizer, transform quantizer at large M, dynamic global scale, MXFP4
+quantizer).  --case runs one kernel a few times on synthetic data, for ncu.
+
 --impl reference times that oracle as the reference arm.  Under torchrun
 (N > 1) every rank runs its own batch (weak scaling, no data-path collective);
 only the barrier and the max-over-ranks time reduction touch the network.
