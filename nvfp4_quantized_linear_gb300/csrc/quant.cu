@@ -1,4 +1,4 @@
-// NVFP4 quantizer kernels: bf16 rows -> packed E2M1 + tiled E4M3 block scales.
+// Quantizer kernels: bf16 rows -> packed E2M1 + tiled block scales.
 //
 // Page "TorchNvFp4LinearKernel" (vLLM PR #53319), section 关键源码片段:
 // apply_weights calls scaled_fp4_quant(x, global_scale, swizzled layout,
@@ -6,6 +6,16 @@
 // the weight.  Page "QUTLASS fusedQuantizeNv" (vLLM PR #43229), 实现拆解 items
 // 3 and 6: an optional block-diagonal transform (1/sqrt(n) folded into it,
 // result in bf16) runs first, fused into the same kernel.
+//
+// Kernels in this file:
+//   quant_kernel               NVFP4 (16-element blocks, E4M3 scales, global scale)
+//   quant_mx_kernel            MXFP4 (32-element blocks, E8M0 scales; page "B12X"'s
+//                              MXFP4 backend)
+//   act_amax_kernel            per-tensor max |x| for the dynamic global scale
+//   act_scale_finalize_kernel  gs = 448 * 6 / amax and alpha from that maximum
+//   quant_transform_kernel     transform on the tensor cores (tcgen05 kind::f16)
+//                              fused with the NVFP4 quantizer; its kAmaxOnly
+//                              variant reduces max |y| for the dynamic scale
 //
 // Per 16-element block (all fp32, round-to-nearest-even, IEEE division):
 //   s = (amax * gs) / 6;  sf = e4m3(s);  inv = sf ? gs / e4m3(sf) : 0;
