@@ -293,8 +293,9 @@ def time_oracle(sample: OracleSample, procs: int, steps: int | None = None, warm
     import multiprocessing as mp
     ctx = mp.get_context("spawn")                 # never fork a process that has touched the GPU
     barrier, results = ctx.Barrier(procs), ctx.Queue()
-    ps = [ctx.Process(target=_oracle_worker,
-                      args=(sample.layers, sample.rows, steps, warmup, min_seconds, barrier, results))
+    # only arrays and scalars go to the processes (no torch import there)
+    layers = [{key: L[key] for key in ("x", "b", "sb", "gs_x", "alpha")} for L in sample.layers]
+    ps = [ctx.Process(target=_oracle_worker, args=(layers, sample.rows, steps, warmup, min_seconds, barrier, results))
           for _ in range(procs)]
     for p in ps:
         p.start()
