@@ -42,6 +42,39 @@ def test_header_declarations_are_all_exported(lib):
     assert sorted(n for n, _, _ in nv.EXPORTS) == names
 
 
+def _prototypes():
+    """name -> parameter count of every function declared in the header."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for name, params in re.findall(r"\b(nvfp4_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", text):
+        params = params.strip()
+        out[name] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_arity_matches_the_header():
+    protos = _prototypes()
+    assert set(protos) == {n for n, _, _ in nv.EXPORTS}
+    for name, _, args in nv.EXPORTS:
+        assert len(args) == protos[name], (name, len(args), protos[name])
+
+
+def test_header_is_plain_c():
+    """include/nvfp4.h compiles as C11 (and as C++17) on its own: a C ABI."""
+    import shutil
+    import subprocess
+    import tempfile
+    if shutil.which("gcc") is None:
+        pytest.skip("no gcc")
+    with tempfile.TemporaryDirectory() as d:
+        src = os.path.join(d, "use.c")
+        with open(src, "w") as f:
+            f.write('#include "nvfp4.h"\nint f(void) { return nvfp4_abi_version() + (int)NVFP4_ERR_ALIAS; }\n')
+        inc = os.path.dirname(HEADER)
+        subprocess.check_call(["gcc", "-std=c11", "-Wall", "-Werror", "-fsyntax-only", "-I", inc, src])
+        subprocess.check_call(["g++", "-std=c++17", "-Wall", "-Werror", "-fsyntax-only", "-x", "c++", "-I", inc, src])
+
+
 def test_abi_version(lib):
     assert nv.nvfp4_abi_version() == 1
 
