@@ -199,6 +199,41 @@ def test_transform_quant_parity(bs, m):
     assert n_bad <= max(2, 1e-4 * (got_pk.size + got_sf.size)), f"{n_bad} bytes differ end to end"
 
 
+def _exact_sum_activation(m: int, k: int, bs: int, seed: int) -> torch.Tensor:
+    """Small integers times a per-row power of two: in every bs-block the first
+    element is odd and the others even, so each y = t * (sum of +-x_i) is an
+    odd multiple of t (never zero, so no sign-of-zero choice arises), and every
+    partial sum of the exact bf16 x bf16 products is exact in fp32 (T's
+    entries all have the magnitude t, and |sum| <= 7 * bs)."""
+    g = torch.Generator().manual_seed(seed)
+    v = torch.randint(-3, 4, (m, k), generator=g) * 2                      # even in [-6, 6]
+    odd = torch.randint(0, 4, (m, k // bs), generator=g) * 2 + 1            # 1, 3, 5, 7
+    sign = torch.randint(0, 2, (m, k // bs), generator=g) * 2 - 1
+    v[:, ::bs] = odd * sign
+    e = torch.randint(-3, 4, (m, 1), generator=g).float()
+    return (v.float() * torch.exp2(e)).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("bs", [16, 32, 64, 128])
+@pytest.mark.parametrize("m", [300, 4096])
+def test_transform_quant_exact_sums_zero_mismatch(bs, m):
+    """Transform inputs whose sums are exact in fp32 (reading A12: the exact
+    case of the tiered parity): whatever order the tensor core sums in, y is
+    the exact sum rounded once, so y, the packed codes and the scales must
+    equal the oracle's end to end with no byte different."""
+    k = 1024
+    x = _exact_sum_activation(m, k, bs, seed=8100 + bs + m)
+    t = syn.random_hadamard_transform(bs, seed=8200 + bs)
+    gs = float(np.float32(syn.E4M3_MAX * syn.FP4_MAX) / np.float32(syn.transformed_amax(x, t)))
+    got_pk, got_sf, y = _gpu_quant_export(x, k, gs, t, bs)
+    rows = np.arange(m) if m <= 300 else sample_indices(m, 64, seed=bs, must=tile_edges(m, 128))
+    y_ref = oracle.transform(syn.bf16_bits(x[torch.from_numpy(rows)]), syn.bf16_bits(t), bs)
+    assert int((y[rows] != y_ref).sum()) == 0, "y differs from the exactly rounded sum"
+    packed, sf_lin = oracle.quantize(y_ref, gs, k=k)
+    assert int((got_pk[rows] != packed).sum()) == 0, "packed codes differ end to end"
+    assert int((gather_scales(got_sf, rows, sf_lin.shape[1], k) != sf_lin).sum()) == 0, "scales differ end to end"
+
+
 @pytest.mark.parametrize("bs", [16, 32, 64, 128])
 def test_transform_quant_full_size_sampled(bs):
     """The transform workload's M = 4096, K = 4096 at full size (32 x 32 tiles
