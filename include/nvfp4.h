@@ -221,6 +221,27 @@ nvfp4_status nvfp4_gemm(const uint8_t *a_fp4, const uint8_t *a_sf, int64_t m,
                         int64_t k, const float *alpha_dev, const void *bias_bf16,
                         void *out_bf16, int64_t ldo, nvfp4_stream_t stream);
 
+/* nvfp4_gemm with the two choices the library otherwise makes itself, for
+ * testing its kernels and its failure path (the pages have no counterpart):
+ *   kernel         0: as nvfp4_gemm (the CTA-pair kernel for m > 128, else the
+ *                     one-CTA kernel);  1: the one-CTA kernel at any m;
+ *                  2: the CTA-pair kernel (m > 128 only, else NVFP4_ERR_INVALID_ARG).
+ *   wait_limit_ns  bound of every pipeline barrier wait of this launch, in
+ *                  [1e6, 1e10] ns; 0 = the library's two seconds.
+ *   drill          0: compute normally.  1: timeout drill -- the kernel's copy
+ *                  producers issue nothing, so each of its barrier waits runs
+ *                  out after wait_limit_ns; the kernel then sets the device
+ *                  error flag (nvfp4_device_error() reports NVFP4_ERR_TIMEOUT)
+ *                  and ends with nothing computed, stored or left in flight,
+ *                  so the next call runs normally.  The call itself returns
+ *                  NVFP4_OK (the wait runs out on the device, after the launch).
+ * Every other argument, check and result is that of nvfp4_gemm. */
+nvfp4_status nvfp4_gemm_ex(const uint8_t *a_fp4, const uint8_t *a_sf, int64_t m,
+                           const uint8_t *w_fp4, const uint8_t *w_sf, int64_t n_w, int64_t n_out,
+                           int64_t k, const float *alpha_dev, const void *bias_bf16,
+                           void *out_bf16, int64_t ldo, int kernel, uint64_t wait_limit_ns, int drill,
+                           nvfp4_stream_t stream);
+
 /* The whole linear layer (torch-backend page apply_weights; b12x page
  * _apply_b12x_nvfp4_linear): nvfp4_quant_act of x into `workspace`, then
  * the GEMM of nvfp4_gemm, all on `stream`.  workspace (device) is scratch owned
@@ -253,7 +274,10 @@ nvfp4_status nvfp4_linear(const void *x_bf16, int64_t m, int64_t k, int64_t ldx,
  *     k = 14336 or m = 8192 at k = 3584 fit.
  *   - The first call on a device looks up the scratch's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is kept with the id of the
+ *     device's CUDA context; after the context is torn down and re-created
+ *     (cudaDeviceReset) the next call looks it up again, so make that call
+ *     outside a capture too.
  *   - It allocates nothing (no cudaMalloc / cudaFree, no allocating library
  *     call).  Every call on a device shares the one scratch array and leaves
  *     its contents behind; calls whose work overlaps on the GPU (e.g. on two

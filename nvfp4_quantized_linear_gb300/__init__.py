@@ -23,7 +23,7 @@ __all__ = [
     "nvfp4_abi_version", "nvfp4_is_supported", "nvfp4_last_error_string", "nvfp4_device_error",
     "nvfp4_packed_bytes", "nvfp4_scale_bytes", "nvfp4_linear_workspace_bytes",
     "nvfp4_prepare_weight", "nvfp4_quant_act", "nvfp4_quant_act_export_y", "nvfp4_act_global_scale", "nvfp4_mxfp4_scale_bytes", "nvfp4_mxfp4_quant_act",
-    "nvfp4_gemm", "nvfp4_linear", "nvfp4_linear_noalloc",
+    "nvfp4_gemm", "nvfp4_gemm_ex", "nvfp4_linear", "nvfp4_linear_noalloc",
     "padded_k", "scale_shape", "quant_act", "quant_act_mx", "prepare_weight", "linear", "act_global_scale",
 ]
 
@@ -54,6 +54,8 @@ EXPORTS = [
     ("nvfp4_mxfp4_scale_bytes", _SZ, [_I64, _I64]),
     ("nvfp4_mxfp4_quant_act", _I32, [_P, _I64, _I64, _I64, _P, _P, _P]),
     ("nvfp4_gemm", _I32, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _P, _P, _I64, _P]),
+    ("nvfp4_gemm_ex", _I32, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _P, _P, _I64, _I32, ctypes.c_uint64, _I32,
+                             _P]),
     ("nvfp4_linear", _I32, [_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _I64, _I64, _P, _P, _P, _I64,
                             _P, _SZ, _P]),
     ("nvfp4_linear_noalloc", _I32, [_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _I64, _I64, _P, _P, _P, _I64,
@@ -201,6 +203,13 @@ def nvfp4_gemm(a_fp4, a_sf, m: int, w_fp4, w_sf, n_w: int, n_out: int, k: int, a
                stream=None) -> None:
     _check(load_library().nvfp4_gemm(_ptr(a_fp4), _ptr(a_sf), m, _ptr(w_fp4), _ptr(w_sf), n_w, n_out, k,
                                      _ptr(alpha), _ptr(bias), _ptr(out), ldo, _stream(stream)))
+
+
+def nvfp4_gemm_ex(a_fp4, a_sf, m: int, w_fp4, w_sf, n_w: int, n_out: int, k: int, alpha, bias, out, ldo: int,
+                  kernel: int = 0, wait_limit_ns: int = 0, drill: int = 0, stream=None) -> None:
+    _check(load_library().nvfp4_gemm_ex(_ptr(a_fp4), _ptr(a_sf), m, _ptr(w_fp4), _ptr(w_sf), n_w, n_out, k,
+                                        _ptr(alpha), _ptr(bias), _ptr(out), ldo, kernel, wait_limit_ns, drill,
+                                        _stream(stream)))
 
 
 def nvfp4_linear(x, m: int, k: int, ldx: int, gs, transform, bs: int, w_fp4, w_sf, n_w: int, n_out: int,

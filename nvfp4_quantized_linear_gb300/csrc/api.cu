@@ -4,7 +4,6 @@
 #include <algorithm>
 #include <cstdarg>
 #include <cstdio>
-#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -16,16 +15,6 @@
 namespace {
 
 thread_local std::string g_last_error;
-
-// GEMMs with m > 128 run on the CTA-pair kernel (256 x 256 tiles, half of B
-// per SM), smaller ones on the one-CTA kernel (which can split K).  Both compute
-// the same result; NVFP4_GEMM_ONE_CTA=1 in the environment (read once, when the
-// library loads) keeps every GEMM on the one-CTA kernel, so that its m > 128
-// path stays testable.
-const bool g_use_pair_kernel = [] {
-    const char *v = getenv("NVFP4_GEMM_ONE_CTA");
-    return !(v != nullptr && v[0] == '1');
-}();
 
 nvfp4_status fail(nvfp4_status st, const char *fmt, ...)
 {
@@ -248,6 +237,8 @@ nvfp4::GemmParams gemm_params(const uint8_t *a_sf, int64_t m, const uint8_t *w_s
     g.stages_per_split = (g.num_k64 + 3) / 4;
     g.partials = nullptr;
     g.part_ld = 0;
+    g.wait_ns = nvfp4::kDefaultWaitNs;
+    g.drill = 0;
     return g;
 }
 
@@ -304,15 +295,22 @@ constexpr size_t kSplitBytesPerRow = 4 * 160 * 256 * sizeof(float);
 // small m it may split K and finish with the reduce kernel.  after_quant: the
 // kernel just before on `s` is the quantizer of `a` (and nothing else), so the
 // GEMM may start as its programmatic dependent.
+// GEMM kernel choice: the CTA-pair kernel (256 x 256 tiles, half of B per SM)
+// for m > 128, the one-CTA kernel (which can split K) otherwise.  Both compute
+// the same result; nvfp4_gemm_ex lets a test pick either.
+enum GemmKernel { kGemmAuto = 0, kGemmOneCta = 1, kGemmPair = 2 };
+
 nvfp4_status run_gemm(const uint8_t *a, const uint8_t *a_sf, int64_t m, const uint8_t *w, const uint8_t *w_sf,
                       int64_t n_w, int64_t n_out, int64_t k, const float *alpha, const void *bias, void *out,
                       int64_t ldo, int num_sms, cudaStream_t s, float *partials = nullptr, size_t partial_bytes = 0,
-                      bool after_quant = false)
+                      bool after_quant = false, int kernel = kGemmAuto, uint64_t wait_ns = 0, int drill = 0)
 {
     unsigned int *err = nullptr;
     cudaError_t e = nvfp4::device_error_word(&err);
     if (e != cudaSuccess) return launch_status(e, "GEMM (error word)");
     nvfp4::GemmParams g = gemm_params(a_sf, m, w_sf, n_w, n_out, k, alpha, bias, out, ldo, err);
+    if (wait_ns != 0) g.wait_ns = wait_ns;
+    g.drill = drill;
     if (partials != nullptr) {
         int sps = 0;
         const int splits = split_k_plan(g, num_sms, &sps);
@@ -324,8 +322,9 @@ nvfp4_status run_gemm(const uint8_t *a, const uint8_t *a_sf, int64_t m, const ui
         }
     }
     const char *why = nullptr;
-    e = (m > 128 && g_use_pair_kernel) ? nvfp4::launch_gemm_pair(g, a, w, num_sms, s, &why, after_quant)
-                                       : nvfp4::launch_gemm(g, a, w, num_sms, s, &why, after_quant);
+    const bool pair = kernel == kGemmPair || (kernel == kGemmAuto && m > 128);
+    e = pair ? nvfp4::launch_gemm_pair(g, a, w, num_sms, s, &why, after_quant)
+             : nvfp4::launch_gemm(g, a, w, num_sms, s, &why, after_quant);
     if (why) return fail(NVFP4_ERR_CUDA, "%s", why);
     nvfp4_status st = launch_status(e, "GEMM kernel");
     if (st != NVFP4_OK || g.splits == 1) return st;
@@ -522,10 +521,19 @@ nvfp4_status nvfp4_prepare_weight(const void *w_bf16, int64_t n, int64_t k, int6
                      reinterpret_cast<cudaStream_t>(stream));
 }
 
-nvfp4_status nvfp4_gemm(const uint8_t *a_fp4, const uint8_t *a_sf, int64_t m, const uint8_t *w_fp4,
-                        const uint8_t *w_sf, int64_t n_w, int64_t n_out, int64_t k, const float *alpha_dev,
-                        const void *bias_bf16, void *out_bf16, int64_t ldo, nvfp4_stream_t stream)
+nvfp4_status nvfp4_gemm_ex(const uint8_t *a_fp4, const uint8_t *a_sf, int64_t m, const uint8_t *w_fp4,
+                           const uint8_t *w_sf, int64_t n_w, int64_t n_out, int64_t k, const float *alpha_dev,
+                           const void *bias_bf16, void *out_bf16, int64_t ldo, int kernel, uint64_t wait_limit_ns,
+                           int drill, nvfp4_stream_t stream)
 {
+    if (kernel < kGemmAuto || kernel > kGemmPair)
+        return fail(NVFP4_ERR_INVALID_ARG, "kernel must be 0 (automatic), 1 (one CTA) or 2 (CTA pair), got %d", kernel);
+    if (kernel == kGemmPair && m > 0 && m <= 128)
+        return fail(NVFP4_ERR_INVALID_ARG, "the CTA-pair kernel needs m > 128 (got %lld)", (long long)m);
+    if (wait_limit_ns != 0 && (wait_limit_ns < 1000000ull || wait_limit_ns > 10000000000ull))
+        return fail(NVFP4_ERR_INVALID_ARG, "wait_limit_ns must be 0 or within [1e6, 1e10] (got %llu)",
+                    (unsigned long long)wait_limit_ns);
+    if (drill != 0 && drill != 1) return fail(NVFP4_ERR_INVALID_ARG, "drill must be 0 or 1 (got %d)", drill);
     nvfp4_status st = check_gemm_args(m > 0 ? a_fp4 : nullptr, m > 0 ? a_sf : nullptr, m, w_fp4, w_sf, n_w, n_out, k,
                                       alpha_dev, bias_bf16, out_bf16, ldo);
     if (st != NVFP4_OK) return st;
@@ -539,7 +547,15 @@ nvfp4_status nvfp4_gemm(const uint8_t *a_fp4, const uint8_t *a_sf, int64_t m, co
     int num_sms = 0;
     if ((st = current_device(&num_sms)) != NVFP4_OK) return st;
     return run_gemm(a_fp4, a_sf, m, w_fp4, w_sf, n_w, n_out, k, alpha_dev, bias_bf16, out_bf16, ldo, num_sms,
-                    reinterpret_cast<cudaStream_t>(stream));
+                    reinterpret_cast<cudaStream_t>(stream), nullptr, 0, false, kernel, wait_limit_ns, drill);
+}
+
+nvfp4_status nvfp4_gemm(const uint8_t *a_fp4, const uint8_t *a_sf, int64_t m, const uint8_t *w_fp4,
+                        const uint8_t *w_sf, int64_t n_w, int64_t n_out, int64_t k, const float *alpha_dev,
+                        const void *bias_bf16, void *out_bf16, int64_t ldo, nvfp4_stream_t stream)
+{
+    return nvfp4_gemm_ex(a_fp4, a_sf, m, w_fp4, w_sf, n_w, n_out, k, alpha_dev, bias_bf16, out_bf16, ldo, kGemmAuto,
+                         0, 0, stream);
 }
 
 nvfp4_status nvfp4_linear(const void *x_bf16, int64_t m, int64_t k, int64_t ldx, const float *gs_dev,

@@ -63,7 +63,11 @@ struct GemmParams {
     int32_t stages_per_split;
     float *partials;
     int64_t part_ld;
+    uint64_t wait_ns;                // bound of every pipeline barrier wait (ns of %globaltimer)
+    int32_t drill;                   // 1: timeout drill, the producers issue no copies (test hook)
 };
+
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;   // two seconds
 
 // Launchers (return a cudaError_t; no host synchronisation).
 cudaError_t launch_quant(const QuantParams &p, int num_sms, cudaStream_t s);

@@ -72,7 +72,6 @@ constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;   // barriers + alignment 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemSf = 256;
 constexpr uint32_t kSfColsPerStage = 48;
-constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kThreads = 512;                 // four warpgroups
 constexpr int kSfWarp0 = 4;                   // warps 4..7: scale staging, lane quarter warp % 4
 constexpr int kEpiWarp0 = 8;                  // warps 8..15: epilogue, lane quarter warp % 4,
@@ -179,9 +178,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int col_base = t.nb * kBN + hcol;
             const uint16_t *s_bias = reinterpret_cast<const uint16_t *>(smem + kOffBias) + (it & 1) * kBN + hcol;
             if (use_bias &&
-                !__all_sync(~0u, mbar_wait(&bias_full[it & 1], (it >> 1) & 1, p.err_flag, kErrTimeout, kWaitNs)))
+                !__all_sync(~0u, mbar_wait(&bias_full[it & 1], (it >> 1) & 1, p.err_flag, kErrTimeout, p.wait_ns)))
                 break;
-            if (!__all_sync(~0u, mbar_wait(tmem_full, acc_phase, p.err_flag, kErrTimeout, kWaitNs))) break;
+            if (!__all_sync(~0u, mbar_wait(tmem_full, acc_phase, p.err_flag, kErrTimeout, p.wait_ns))) break;
             tc_fence_after_sync();
             acc_phase ^= 1;
             const int64_t row = (int64_t)t.mb * kBM + q * 32 + lane;
@@ -287,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
             const Work wk = work_of(tile, p, num_ks);
             for (int ks = wk.ks0; ks < wk.ks1; ++ks) {
-                ok = __all_sync(~0u, mbar_wait(&full[stage], phase, p.err_flag, kErrTimeout, kWaitNs));
+                ok = __all_sync(~0u, mbar_wait(&full[stage], phase, p.err_flag, kErrTimeout, p.wait_ns));
                 if (!ok) break;
                 uint32_t a[16], b[32];
 #pragma unroll
@@ -316,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         setmaxnreg_dec<kRegsCtl>();
-        if ((warp == 0 || warp == 3) && lane == 0) {
+        if ((warp == 0 || warp == 3) && lane == 0 && !p.drill) {   // (a timeout drill issues no copies)
             // ----------------------------------------------------- producers --
             // Two threads fill the ring, each with its half of every stage:
             // warp 0 the activation side (A tile + its scale tile), warp 3 the
@@ -340,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Tile t = wk.t;
                 const int halves = min(kBN, p.n_out - t.nb * kBN) > 128 ? 2 : 1;
                 for (int ks = wk.ks0; ks < wk.ks1; ++ks) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1, p.err_flag, kErrTimeout, kWaitNs)) { ok = false; break; }
+                    if (!mbar_wait(&empty[stage], phase ^ 1, p.err_flag, kErrTimeout, p.wait_ns)) { ok = false; break; }
                     const uint32_t sf_bytes = (uint32_t)min(4, p.num_k64 - ks * 4) * 512;
                     if (act_side) {
                         mbar_arrive_expect_tx(&full[stage], kABytes + sf_bytes);
@@ -364,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Every copy this thread issued has landed before the CTA may exit.
             for (int s = 0; s < kStages; ++s)
                 if (issued_mask & (1u << s))
-                    mbar_wait(&full[s], (issued_phase >> s) & 1u, p.err_flag, kErrTimeout, kWaitNs);
+                    mbar_wait(&full[s], (issued_phase >> s) & 1u, p.err_flag, kErrTimeout, p.wait_ns);
         } else if (warp == 2 && p.splits == 1 && p.bias != nullptr) {
             // ---------------------------------------------------- bias loader --
             // The bias of each tile into one of two shared buffers, for the
@@ -376,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int n_rows = min(kBN, p.n_out - t.nb * kBN);
                 const int b = it & 1;
                 if (!__all_sync(~0u, mbar_wait(&bias_empty[b], ((it >> 1) & 1) ^ 1, p.err_flag, kErrTimeout,
-                                               kWaitNs)))
+                                               p.wait_ns)))
                     break;
                 for (int j = lane; j < kBN; j += 32)
                     s_bias_all[b * kBN + j] = (j < n_rows) ? p.bias[t.nb * kBN + j] : (uint16_t)0;
@@ -398,12 +397,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Work wk = work_of(tile, p, num_ks);
                 const int n_rows = min(kBN, p.n_out - wk.t.nb * kBN);
                 const uint32_t idesc = n_rows > 128 ? idesc_nvf4(128, 256) : idesc_nvf4(128, 128);
-                if (!__all_sync(~0u, mbar_wait(tmem_empty, acc_phase ^ 1, p.err_flag, kErrTimeout, kWaitNs))) break;
+                if (!__all_sync(~0u, mbar_wait(tmem_empty, acc_phase ^ 1, p.err_flag, kErrTimeout, p.wait_ns))) break;
                 tc_fence_after_sync();
                 for (int ks = wk.ks0; ks < wk.ks1; ++ks) {
                     // sf_ready implies full: the scale warps arrive on it only
                     // after they saw the stage land (and read its scales).
-                    if (!__all_sync(~0u, mbar_wait(&sf_ready[stage], phase, p.err_flag, kErrTimeout, kWaitNs))) {
+                    if (!__all_sync(~0u, mbar_wait(&sf_ready[stage], phase, p.err_flag, kErrTimeout, p.wait_ns))) {
                         ok = false;
                         break;
                     }
@@ -430,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // No MMA may still be running when the TMEM is released.
             if (leader) tc_commit(mma_done);
             __syncwarp();
-            mbar_wait(mma_done, 0, p.err_flag, kErrTimeout, kWaitNs);
+            mbar_wait(mma_done, 0, p.err_flag, kErrTimeout, p.wait_ns);
         }
     }
 

@@ -59,7 +59,6 @@ constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;         // barriers + alig
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemSf = 256;
 constexpr uint32_t kSfColsPerStage = 48;
-constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kThreads = 512;
 constexpr int kSfWarp0 = 4;
 constexpr int kEpiWarp0 = 8;
@@ -146,9 +145,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int col_base = t.nb * kTileN + hcol;
             const uint16_t *s_bias = reinterpret_cast<const uint16_t *>(smem + kOffBias) + (it & 1) * kTileN + hcol;
             if (use_bias &&
-                !__all_sync(~0u, mbar_wait(&bias_full[it & 1], (it >> 1) & 1, p.err_flag, kErrTimeout, kWaitNs)))
+                !__all_sync(~0u, mbar_wait(&bias_full[it & 1], (it >> 1) & 1, p.err_flag, kErrTimeout, p.wait_ns)))
                 break;
-            if (!__all_sync(~0u, mbar_wait(tmem_full, acc_phase, p.err_flag, kErrTimeout, kWaitNs))) break;
+            if (!__all_sync(~0u, mbar_wait(tmem_full, acc_phase, p.err_flag, kErrTimeout, p.wait_ns))) break;
             tc_fence_after_sync();
             acc_phase ^= 1;
 
@@ -223,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int tile = pair_id; tile < num_tiles && ok; tile += num_pairs) {
             for (int ks = 0; ks < num_ks; ++ks) {
-                ok = __all_sync(~0u, mbar_wait(&full[stage], phase, p.err_flag, kErrTimeout, kWaitNs));
+                ok = __all_sync(~0u, mbar_wait(&full[stage], phase, p.err_flag, kErrTimeout, p.wait_ns));
                 if (!ok) break;
                 uint32_t a[16], b[32];
 #pragma unroll
@@ -255,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         setmaxnreg_dec<kRegsCtl>();
-        if ((warp == 0 || warp == 3) && lane == 0) {
+        if ((warp == 0 || warp == 3) && lane == 0 && !p.drill) {   // (a timeout drill issues no copies)
             // ----------------------------------------------------- producers --
             // Two threads per CTA fill the ring, each with its half of every
             // stage and one arrival on `full` (count 2): warp 0 this CTA's A
@@ -275,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool a_here = band_a < a_bands;
                 const int halves = min(kTileN, p.n_out - t.nb * kTileN) > 128 ? 2 : 1;
                 for (int ks = 0; ks < num_ks; ++ks) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1, p.err_flag, kErrTimeout, kWaitNs)) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1, p.err_flag, kErrTimeout, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -303,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             for (int s = 0; s < kStages; ++s)
                 if (issued_mask & (1u << s))
-                    mbar_wait(&full[s], (issued_phase >> s) & 1u, p.err_flag, kErrTimeout, kWaitNs);
+                    mbar_wait(&full[s], (issued_phase >> s) & 1u, p.err_flag, kErrTimeout, p.wait_ns);
         } else if (warp == 2 && p.bias != nullptr) {
             // ---------------------------------------------------- bias loader --
             uint16_t *s_bias_all = reinterpret_cast<uint16_t *>(smem + kOffBias);
@@ -313,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int n_rows = min(kTileN, p.n_out - t.nb * kTileN);
                 const int b = it & 1;
                 if (!__all_sync(~0u, mbar_wait(&bias_empty[b], ((it >> 1) & 1) ^ 1, p.err_flag, kErrTimeout,
-                                               kWaitNs)))
+                                               p.wait_ns)))
                     break;
                 for (int j = lane; j < kTileN; j += 32)
                     s_bias_all[b * kTileN + j] = (j < n_rows) ? p.bias[t.nb * kTileN + j] : (uint16_t)0;
@@ -332,11 +331,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idesc = idesc_nvf4(kTileM, kTileN);
             bool ok = true;
             for (int tile = pair_id; tile < num_tiles && ok; tile += num_pairs) {
-                if (!__all_sync(~0u, mbar_wait(tmem_empty, acc_phase ^ 1, p.err_flag, kErrTimeout, kWaitNs)))
+                if (!__all_sync(~0u, mbar_wait(tmem_empty, acc_phase ^ 1, p.err_flag, kErrTimeout, p.wait_ns)))
                     break;
                 tc_fence_after_sync();
                 for (int ks = 0; ks < num_ks; ++ks) {
-                    if (!__all_sync(~0u, mbar_wait(&sf_ready[stage], phase, p.err_flag, kErrTimeout, kWaitNs))) {
+                    if (!__all_sync(~0u, mbar_wait(&sf_ready[stage], phase, p.err_flag, kErrTimeout, p.wait_ns))) {
                         ok = false;
                         break;
                     }
@@ -360,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (issuer) tc_commit_pair(mma_done);
             __syncwarp();
-            mbar_wait(mma_done, 0, p.err_flag, kErrTimeout, kWaitNs);
+            mbar_wait(mma_done, 0, p.err_flag, kErrTimeout, p.wait_ns);
         }
     }
 
