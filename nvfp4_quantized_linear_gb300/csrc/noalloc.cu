@@ -11,13 +11,19 @@
 // The scratch is a file-scope __device__ array of kScratchBytes (16 MiB).
 // Every GPU that loads the library holds it until the process exits.  In host
 // code the array's name is only a host-side stand-in, never a device address:
-// the device address is looked up once per device with cudaGetSymbolAddress
-// on the first call made on that device (with that device current), checked,
-// and cached.  That first call should therefore come before any stream
-// capture.  All calls on a device share the one array, so calls whose work
-// overlaps on the GPU (for instance on two streams) race on it.
+// the device address is looked up with cudaGetSymbolAddress, with the device
+// current, by the first call made on that device, checked, and kept.  That
+// first call should therefore come before any stream capture.  The address
+// belongs to the device's current CUDA context: if that context is torn down
+// and re-created (cudaDeviceReset), the module holding the array is loaded
+// again and may sit elsewhere, so the kept address is tagged with the
+// context's id and the look-up is repeated when the id changes.  All calls on
+// a device share the one array, so calls whose work overlaps on the GPU (for
+// instance on two streams) race on it.
 #include <cstdio>
 #include <mutex>
+
+#include <cudaTypedefs.h>
 
 #include "common.cuh"
 #include "nvfp4.h"
@@ -32,7 +38,11 @@ constexpr size_t kScratchBytes = size_t(16) << 20;   // 16 MiB
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
-void *g_scratch_ptr[kMaxDevices] = {nullptr};
+struct ScratchSlot {
+    void *ptr = nullptr;                  // device address of g_noalloc_scratch
+    unsigned long long ctx_id = 0;        // id of the context it was looked up in
+};
+ScratchSlot g_scratch[kMaxDevices];
 std::mutex g_scratch_mutex;
 
 nvfp4_status noalloc_fail(nvfp4_status st, const char *msg)
@@ -40,7 +50,32 @@ nvfp4_status noalloc_fail(nvfp4_status st, const char *msg)
     return static_cast<nvfp4_status>(nvfp4::record_error(st, msg));
 }
 
-// Device address of this device's scratch array (looked up on first use).
+// Id of the calling thread's current CUDA context (the device's primary
+// context once the runtime has set it up), through the driver entry points
+// the runtime exposes; false if it cannot be read.
+bool current_context_id(unsigned long long *id)
+{
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+        cudaGetLastError();
+    });
+    CUcontext ctx = nullptr;
+    return get_current != nullptr && get_id != nullptr && get_current(&ctx) == CUDA_SUCCESS && ctx != nullptr &&
+           get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of this device's scratch array: looked up on the first call
+// made on the device, and again whenever the device's context has changed.
 nvfp4_status scratch_address(void **ptr)
 {
     int dev = -1;
@@ -49,8 +84,14 @@ nvfp4_status scratch_address(void **ptr)
         cudaGetLastError();
         return noalloc_fail(NVFP4_ERR_CUDA, "nvfp4_linear_noalloc: cannot determine the current CUDA device");
     }
+    // A thread that has made no runtime call needing the context yet may have
+    // none current; the symbol look-up below then makes the device's primary
+    // context current, and its id is read after it.
+    unsigned long long ctx = 0;
+    const bool have_ctx = current_context_id(&ctx);
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (g_scratch_ptr[dev] == nullptr) {
+    ScratchSlot &slot = g_scratch[dev];
+    if (!have_ctx || slot.ptr == nullptr || slot.ctx_id != ctx) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || p == nullptr) {
@@ -60,9 +101,12 @@ nvfp4_status scratch_address(void **ptr)
                      cudaGetErrorString(e));
             return noalloc_fail(NVFP4_ERR_CUDA, msg);
         }
-        g_scratch_ptr[dev] = p;
+        if (!current_context_id(&ctx))
+            return noalloc_fail(NVFP4_ERR_CUDA, "nvfp4_linear_noalloc: cannot identify the current CUDA context");
+        slot.ptr = p;
+        slot.ctx_id = ctx;
     }
-    *ptr = g_scratch_ptr[dev];
+    *ptr = slot.ptr;
     return NVFP4_OK;
 }
 
