@@ -1,16 +1,22 @@
 """Benchmark of the NVFP4 W4A4 linear on GB300 (one JSON line on rank 0).
 
 A step is one pass of the whole hot path over one batch: the four decoder
-linears of a Llama-3.1-8B-shaped layer (qkv 4096->6144, o 4096->4096,
-gate_up 4096->28672, down 14336->4096) at M = 8192 tokens, each through
-nvfp4_linear (activation quantization + block-scaled FP4 GEMM with the
-alpha/bias/bf16 epilogue).  Weights are prepared once, outside the timed region.
+linears of a Qwen3-32B-shaped layer (qkv 5120->10240, o 8192->5120,
+gate_up 5120->51200, down 25600->5120) at M = 16384 tokens, activations with
+0.1% outlier channels scaled x50, each through nvfp4_linear (activation
+quantization + block-scaled FP4 GEMM with the alpha/bias/bf16 epilogue).  This
+is the largest layer workload that fits one GPU.  Weights are prepared once,
+outside the timed region.  --workload llama times the Llama-3.1-8B-shaped
+layer (qkv 4096->6144, o 4096->4096, gate_up 4096->28672, down 14336->4096)
+at M = 8192 instead; the default line also carries that step as
+`llama_m8192`.
 
   value      whole-job NVFP4-linear throughput, sum(2*M*N*K) / time, with the
-             inputs resident in HBM (per-rank inputs of 0.4 GB: larger than L2)
+             inputs resident in HBM (per-rank inputs of 1.4 GB: larger than L2)
   roofline   the GEMM kernel: its algorithmic FLOPs / its own CUDA-event time,
-             against the dense-FP4 peak (measured bf16 peak x the nominal
-             FP4:bf16 ratio 13.5/2.25 = 6)
+             against the dense-FP4 peak (measured burst bf16 peak x the
+             nominal FP4:bf16 ratio 13.5/2.25 = 6: the kernel is timed by CUDA
+             events inside a sub-second region)
   act_quant  the activation quantizer: algorithmic bytes / its CUDA-event time
              with a cold, clean L2 (a 256 MB read before each launch), against the
              measured HBM copy bandwidth; `in_pipeline` gives the same kernel timed
@@ -48,14 +54,19 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "NVFP4 linear TFLOP/s (frac of FP4 peak); act-quant GB/s (frac of HBM peak)"
-WORKLOAD_M = 8192
+# name -> (description, default tokens per GPU, problem generator of synthetic.py)
+WORKLOADS = {
+    "qwen": ("qwen3-32b decoder linears qkv/o/gate_up/down, 0.1% outlier channels x50", 16384, "qwen"),
+    "llama": ("llama3.1-8b decoder linears qkv/o/gate_up/down", 8192, "llama"),
+}
+DEFAULT_WORKLOAD = "qwen"
 FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense FP4 : bf16 tensor rate of GB300
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 CPU_SAMPLE_ROWS = 16                 # cpu_baseline sample: rows x columns of every linear
 CPU_SAMPLE_COLS = 1024
 REF_STEP_ROWS = CPU_SAMPLE_ROWS      # reference arm: the cpu_baseline sample, one per step
 REF_STEP_COLS = CPU_SAMPLE_COLS
-PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "gemm_llama_m8192_traffic.txt")
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "gemm_qwen_gate_up_m16384_traffic.txt")
 
 
 # ------------------------------------------------------------ host logic ----
@@ -66,7 +77,8 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--m", type=int, default=WORKLOAD_M, help="tokens per rank")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--m", type=int, default=None, help="tokens per rank (default: the workload's)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
@@ -81,6 +93,8 @@ def parse_args(argv=None):
                          "(Llama/Qwen/padded-K/transform) and per point of the quantization sweep")
     a = ap.parse_args(argv)
     a.warmup = max(a.warmup, 3)
+    if a.m is None:
+        a.m = WORKLOADS[a.workload][1] if not a.case else 8192
     return a
 
 
@@ -110,12 +124,15 @@ def aggregate(per_rank_units: float, world: int, max_seconds: float) -> float:
     return per_rank_units * world / max_seconds
 
 
-def layer_problems(m: int, rank: int = 0):
+def layer_problems(workload: str, m: int, rank: int = 0):
     from nvfp4_quantized_linear_gb300 import synthetic as syn
-    out = []
-    for p in syn.llama([m]):
-        out.append(syn.Problem(p.workload, p.name, p.m, p.k, p.n, seed=rank_seed(p.seed, rank)))
-    return out
+    make = getattr(syn, WORKLOADS[workload][2])
+    return [syn.Problem(p.workload, p.name, p.m, p.k, p.n, seed=rank_seed(p.seed, rank), x_kind=p.x_kind)
+            for p in make([m])]
+
+
+def workload_label(workload: str, m: int) -> str:
+    return f"{WORKLOADS[workload][0]}, M={m} tokens per GPU"
 
 
 def quant_bytes(m: int, k: int) -> int:
@@ -153,17 +170,25 @@ def gemm_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
-    """DRAM bytes of one gate_up GEMM launch from the committed ncu summary, if
-    it was taken on the current GEMM source; else None."""
+def read_traffic_record(path: str = None):
+    """(gemm_source_hash, DRAM bytes per launch) of a committed ncu traffic
+    summary, or None if it is missing or unreadable."""
     try:
-        with open(PROFILE_TRAFFIC) as f:
+        with open(path or PROFILE_TRAFFIC) as f:
             kv = dict(line.split(":", 1) for line in f if ":" in line and not line.startswith("#"))
-        if kv.get("gemm_source_hash", "").strip() != gemm_source_hash():
-            return None
-        return float(kv["dram_bytes_per_launch_gate_up"].strip())
+        return kv["gemm_source_hash"].strip(), float(kv["dram_bytes_per_launch"].strip())
     except (OSError, KeyError, ValueError):
         return None
+
+
+def recorded_traffic():
+    """DRAM bytes of one gate_up GEMM launch of the headline workload from the
+    committed ncu summary, if it was taken on the current GEMM source; else
+    None (a record of another kernel revision says nothing about this one)."""
+    rec = read_traffic_record()
+    if rec is None or rec[0] != gemm_source_hash():
+        return None
+    return rec[1]
 
 
 class ClockSampler:
@@ -309,31 +334,14 @@ def time_oracle(sample: OracleSample, procs: int, steps: int | None = None, warm
 
 # ------------------------------------------------------------------ GPU ----
 
-def run_ours(args, rank, world, local_rank):
+def setup_layers(problems, dev):
+    """Device tensors of every layer problem: activation, prepared weight,
+    scales, workspace (whose head doubles as the quantizer's output in the
+    per-kernel pass) and output."""
     import torch
-    import torch.distributed as dist
 
     import nvfp4_quantized_linear_gb300 as nv
     from nvfp4_quantized_linear_gb300 import synthetic as syn
-
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    nv.build()
-    ok, why = nv.nvfp4_is_supported(local_rank)
-    if not ok:
-        raise RuntimeError(why)
-    peaks, peak_src = load_peaks()
-    fp4_peak = peaks["bf16_tflops_sustained"] * FP4_OVER_BF16
-    fp4_peak_burst = peaks["bf16_tflops"] * FP4_OVER_BF16
-
-    def barrier():
-        if world > 1:
-            dist.barrier()
-
-    def slowest(v: float) -> float:
-        return max_over_ranks(v, dev)
-
-    problems = layer_problems(args.m, rank)
     layers = []
     for p in problems:
         L = syn.make_layer(p, device=dev)
@@ -350,8 +358,17 @@ def run_ours(args, rank, world, local_rank):
                            a_sf=a_sf, out=out))
         del L
     torch.cuda.synchronize()
-    stream = torch.cuda.current_stream().cuda_stream
-    flops_step = sum(l["p"].flops for l in layers)
+    return layers
+
+
+def measure_step(layers, args, stream, barrier):
+    """(A) the step through nvfp4_linear, K times: its time per step; (B) the
+    same kernels launched one by one, each bracketed by CUDA events on the
+    launching stream: per-kernel durations; (C) the quantizer alone with a
+    cold, clean L2.  Returns the times in seconds."""
+    import torch
+
+    import nvfp4_quantized_linear_gb300 as nv
 
     def linear(l):
         p = l["p"]
@@ -372,86 +389,128 @@ def run_ours(args, rank, world, local_rank):
             linear(l)
     torch.cuda.synchronize()
     nv.nvfp4_device_error()
+    # (A)
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        for l in layers:
+            linear(l)
+    e1.record()
+    torch.cuda.synchronize()
+    barrier()
+    t_step = e0.elapsed_time(e1) / 1e3 / args.steps
+    # (B)
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in layers] for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    for s in range(args.steps):
+        for i, l in enumerate(layers):
+            split(l, evs[s][i])
+    torch.cuda.synchronize()
+    barrier()
+    # (C) reading 256 MB first evicts what the previous kernel left (the GEMM's
+    # dirty output would otherwise be written back while the quantizer streams)
+    cold = torch.empty(64 << 20, dtype=torch.float32, device=layers[0]["x"].device)
+    cold.zero_()
+    cold.sum()                          # writes the zeros back: later reads leave clean lines
+    qevs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in layers]
+            for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for s in range(args.steps):
+        for i, l in enumerate(layers):
+            p = l["p"]
+            cold.sum()
+            qevs[s][i][0].record()
+            nv.nvfp4_quant_act(l["x"], p.m, p.k, p.k, l["gs_x"], None, 0, l["a_fp4"], l["a_sf"], stream)
+            qevs[s][i][1].record()
+    torch.cuda.synchronize()
+    del cold
+    nv.nvfp4_device_error()
+    n = len(layers)
+    return {
+        "step": t_step,
+        "quant": [sum(evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(args.steps)) / args.steps / 1e3
+                  for i in range(n)],
+        "gemm": [sum(evs[s][i][1].elapsed_time(evs[s][i][2]) for s in range(args.steps)) / args.steps / 1e3
+                 for i in range(n)],
+        "quant_cold": [sum(qevs[s][i][0].elapsed_time(qevs[s][i][1]) for s in range(args.steps)) / args.steps / 1e3
+                       for i in range(n)],
+    }
 
+
+def per_layer_rows(layers, t):
+    return [{"layer": l["p"].name, "m": l["p"].m, "k": l["p"].k, "n": l["p"].n,
+             "quant_us": round(tq * 1e6, 2), "quant_us_in_pipeline": round(tqp * 1e6, 2),
+             "gemm_us": round(tg * 1e6, 2), "gemm_tflops": round(l["p"].flops / tg / 1e12, 1),
+             "quant_gbs": round(quant_bytes(l["p"].m, l["p"].k) / tq / 1e9, 1)}
+            for l, tq, tqp, tg in zip(layers, t["quant_cold"], t["quant"], t["gemm"])]
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import nvfp4_quantized_linear_gb300 as nv
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    nv.build()
+    ok, why = nv.nvfp4_is_supported(local_rank)
+    if not ok:
+        raise RuntimeError(why)
+    peaks, peak_src = load_peaks()
+    fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16                 # burst: kernels timed in a sub-second region
+    fp4_peak_sustained = peaks["bf16_tflops_sustained"] * FP4_OVER_BF16
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def slowest(v: float) -> float:
+        return max_over_ranks(v, dev)
+
+    layers = setup_layers(layer_problems(args.workload, args.m, rank), dev)
+    stream = torch.cuda.current_stream().cuda_stream
+    flops_step = sum(l["p"].flops for l in layers)
     sampler = ClockSampler(local_rank)
     with sampler:
-        # (A) the step through nvfp4_linear: value and ms_per_step
-        barrier()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(args.steps):
-            for l in layers:
-                linear(l)
-        e1.record()
-        torch.cuda.synchronize()
-        barrier()
-        t_step = e0.elapsed_time(e1) / 1e3 / args.steps
-        # (B) the same kernels launched one by one, each bracketed by events on
-        # the launching stream: per-kernel durations for the roofline
-        evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in layers]
-               for _ in range(args.steps)]
-        barrier()
-        torch.cuda.synchronize()
-        for s in range(args.steps):
-            for i, l in enumerate(layers):
-                split(l, evs[s][i])
-        torch.cuda.synchronize()
-        barrier()
-        # (C) the quantizer alone with a cold, clean L2: reading 256 MB first
-        # evicts what the previous kernel left (the GEMM's dirty output would
-        # otherwise be written back while the quantizer streams)
-        cold = torch.empty(64 << 20, dtype=torch.float32, device=dev)
-        cold.zero_()
-        cold.sum()                          # writes the zeros back: later reads leave clean lines
-        qevs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in layers]
-                for _ in range(args.steps)]
-        torch.cuda.synchronize()
-        for s in range(args.steps):
-            for i, l in enumerate(layers):
-                p = l["p"]
-                cold.sum()
-                qevs[s][i][0].record()
-                nv.nvfp4_quant_act(l["x"], p.m, p.k, p.k, l["gs_x"], None, 0, l["a_fp4"], l["a_sf"], stream)
-                qevs[s][i][1].record()
-        torch.cuda.synchronize()
-        del cold
-    nv.nvfp4_device_error()
+        t = measure_step(layers, args, stream, barrier)
     clocks = sampler.summary()
 
-    t_quant = [sum(evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(args.steps)) / args.steps / 1e3
-               for i in range(len(layers))]
-    t_gemm = [sum(evs[s][i][1].elapsed_time(evs[s][i][2]) for s in range(args.steps)) / args.steps / 1e3
-              for i in range(len(layers))]
-    t_quant_cold = [sum(qevs[s][i][0].elapsed_time(qevs[s][i][1]) for s in range(args.steps)) / args.steps / 1e3
-                    for i in range(len(layers))]
-    t_step_max = slowest(t_step)
+    t_step_max = slowest(t["step"])
     value = aggregate(flops_step, world, t_step_max) / 1e12
-    gemm_tflops = sum(l["p"].flops for l in layers) / sum(t_gemm) / 1e12
-    top = max(range(len(layers)), key=lambda i: t_gemm[i])          # the dominant launch (gate_up)
-    top_tflops = layers[top]["p"].flops / t_gemm[top] / 1e12
+    gemm_tflops = flops_step / sum(t["gemm"]) / 1e12
+    top = max(range(len(layers)), key=lambda i: t["gemm"][i])          # the dominant launch (gate_up)
+    top_tflops = layers[top]["p"].flops / t["gemm"][top] / 1e12
     q_bytes = sum(quant_bytes(l["p"].m, l["p"].k) for l in layers)
-    quant_gbs = q_bytes / sum(t_quant_cold) / 1e9
-    quant_gbs_pipe = q_bytes / sum(t_quant) / 1e9
-    traffic = recorded_traffic()
+    quant_gbs = q_bytes / sum(t["quant_cold"]) / 1e9
+    quant_gbs_pipe = q_bytes / sum(t["quant"]) / 1e9
+    traffic = recorded_traffic() if (args.workload, args.m) == (DEFAULT_WORKLOAD, WORKLOADS[DEFAULT_WORKLOAD][1]) \
+        else None
+    top_kernel = "gemm_nvf4_pair_kernel" if layers[top]["p"].m > 128 else "gemm_nvf4_kernel"
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_step_max * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4",
         "data": "synthetic",
-        "config": {"workload": f"llama3.1-8b decoder linears qkv/o/gate_up/down, M={args.m} tokens per GPU",
+        "config": {"workload": workload_label(args.workload, args.m),
                    "m": args.m, "layers": [[l["p"].name, l["p"].k, l["p"].n] for l in layers],
-                   "l2": "inputs larger than L2 (0.4 GB of activations per step)", "bias": False,
-                   "transform": None},
-        "roofline": {"bound": "tensor", "kernel": f"gemm_nvf4_pair_kernel ({layers[top]['p'].name} launch)",
+                   "l2": f"inputs larger than L2 ({sum(l['x'].numel() * 2 for l in layers) / 1e9:.2f} GB of "
+                         "activations per step)", "bias": False, "transform": None},
+        "roofline": {"bound": "tensor", "kernel": f"{top_kernel} ({layers[top]['p'].name} launch)",
                      "achieved": round(top_tflops, 2), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
                      "frac": round(top_tflops / fp4_peak, 4),
                      "traffic": (round(traffic) if traffic else None),
                      "algorithmic_bytes": gemm_bytes(layers[top]["p"]),
+                     "flops_per_launch": layers[top]["p"].flops,
                      "all_gemm_launches_achieved": round(gemm_tflops, 2),
-                     "peak_note": (f"dense FP4 = sustained bf16 {peaks['bf16_tflops_sustained']} x {FP4_OVER_BF16:g} "
-                                   f"from {peak_src}; burst-based {fp4_peak_burst:.0f}, nominal 13500"),
+                     "peak_note": (f"dense FP4 = burst bf16 {peaks['bf16_tflops']} x {FP4_OVER_BF16:g} from "
+                                   f"{peak_src}, the figure for a kernel timed alone by CUDA events; "
+                                   f"sustained-based {fp4_peak_sustained:.0f}, nominal 13500"),
+                     "frac_of_sustained": round(top_tflops / fp4_peak_sustained, 4),
                      "frac_of_nominal_13p5": round(top_tflops / 13500.0, 4)},
         "act_quant": {"bound": "hbm", "kernel": "quant_kernel", "achieved": round(quant_gbs, 1),
                       "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(quant_gbs / peaks["hbm_gbs"], 4),
@@ -461,24 +520,37 @@ def run_ours(args, rank, world, local_rank):
                                       "frac": round(quant_gbs_pipe / peaks["hbm_gbs"], 4),
                                       "note": "each launch right after the previous layer's GEMM, whose output "
                                               "is still being written back from L2"}},
-        "per_layer": [{"layer": l["p"].name, "m": l["p"].m, "k": l["p"].k, "n": l["p"].n,
-                       "quant_us": round(tq * 1e6, 2), "quant_us_in_pipeline": round(tqp * 1e6, 2),
-                       "gemm_us": round(tg * 1e6, 2),
-                       "gemm_tflops": round(l["p"].flops / tg / 1e12, 1),
-                       "quant_gbs": round(quant_bytes(l["p"].m, l["p"].k) / tq / 1e9, 1)}
-                      for l, tq, tqp, tg in zip(layers, t_quant_cold, t_quant, t_gemm)],
+        "per_layer": per_layer_rows(layers, t),
         "gpu_launches": 2 * len(layers) * args.steps,
         "clocks": clocks,
     }
 
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, layers, flops_step, barrier, slowest, world, stream)
-    if not args.no_sweep:
-        result["m_sweep"] = run_sweep(args, rank, dev, stream)
     del layers
     torch.cuda.empty_cache()
+    if args.workload == DEFAULT_WORKLOAD and not args.no_sweep:
+        # the Llama-3.1-8B-shaped step at M = 8192 (the smaller prefill workload)
+        sec = setup_layers(layer_problems("llama", 8192, rank), dev)
+        sampler2 = ClockSampler(local_rank)
+        with sampler2:
+            t2 = measure_step(sec, args, stream, barrier)
+        f2 = sum(l["p"].flops for l in sec)
+        top2 = max(range(len(sec)), key=lambda i: t2["gemm"][i])
+        result["llama_m8192"] = {
+            "workload": workload_label("llama", 8192),
+            "value": round(aggregate(f2, world, slowest(t2["step"])) / 1e12, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(t2["step"] * 1e3, 4),
+            "gate_up_gemm_tflops": round(sec[top2]["p"].flops / t2["gemm"][top2] / 1e12, 2),
+            "gate_up_frac": round(sec[top2]["p"].flops / t2["gemm"][top2] / 1e12 / fp4_peak, 4),
+            "per_layer": per_layer_rows(sec, t2), "clocks": sampler2.summary()}
+        result["gpu_launches"] += 2 * len(sec) * args.steps
+        del sec
+        torch.cuda.empty_cache()
+    if not args.no_sweep:
+        result["m_sweep"] = run_sweep(args, rank, dev, stream)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        sample = OracleSample(layer_problems(args.m, 0), CPU_SAMPLE_ROWS, CPU_SAMPLE_COLS)
+        sample = OracleSample(layer_problems(args.workload, args.m, 0), CPU_SAMPLE_ROWS, CPU_SAMPLE_COLS)
         cores = host_cores()
         v, el, reps = time_oracle(sample, cores)
         result["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
@@ -525,8 +597,8 @@ def run_e2e(args, layers, flops_step, barrier, slowest, world, stream):
 
 
 def run_sweep(args, rank, dev, stream):
-    """Decode/prefill-size breakdown: the same four linears at smaller M (not the
-    headline value)."""
+    """Decode/prefill-size breakdown: the four Llama-3.1-8B-shaped linears at
+    smaller M (not the headline value)."""
     import torch
 
     import nvfp4_quantized_linear_gb300 as nv
@@ -535,7 +607,7 @@ def run_sweep(args, rank, dev, stream):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     for m in [1, 16, 128, 1024]:
         layers = []
-        for p in layer_problems(m, rank):
+        for p in layer_problems("llama", m, rank):
             L = syn.make_layer(p, device=dev)
             gs_x = torch.tensor([L.gs_x], dtype=torch.float32, device=dev)
             alpha = torch.tensor([L.alpha], dtype=torch.float32, device=dev)
@@ -567,7 +639,7 @@ def run_sweep(args, rank, dev, stream):
         flops = sum(p.flops for p, *_ in layers)
         wbytes = sum(w.numel() + s.numel() for _, _, _, _, w, s, _, _ in layers)
         abytes = sum(quant_bytes(p.m, p.k) + 2 * p.m * p.n for p, *_ in layers)
-        out.append({"m": m, "us_per_step": round(t * 1e6, 2), "tflops": round(flops / t / 1e12, 2),
+        out.append({"workload": "llama3.1-8b", "m": m, "us_per_step": round(t * 1e6, 2), "tflops": round(flops / t / 1e12, 2),
                     "algorithmic_gbs": round((wbytes + abytes) / t / 1e9, 1), "l2": "flushed before each step"})
         del layers
     return out
@@ -713,7 +785,7 @@ def run_reference(args, rank, world):
     the same workload per step (rank 0 only)."""
     if rank != 0:
         return None
-    sample = OracleSample(layer_problems(args.m, 0), REF_STEP_ROWS, REF_STEP_COLS)
+    sample = OracleSample(layer_problems(args.workload, args.m, 0), REF_STEP_ROWS, REF_STEP_COLS)
     cores = host_cores()
     value, el, _ = time_oracle(sample, cores, steps=args.steps, warmup=args.warmup)
     desc = (f"{REF_STEP_ROWS} rows x {REF_STEP_COLS} output columns of each of the 4 linears "
@@ -722,8 +794,7 @@ def run_reference(args, rank, world):
     return {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": f"llama3.1-8b decoder linears qkv/o/gate_up/down, M={args.m} tokens per GPU",
-                       "m": args.m, "sample": desc},
+            "config": {"workload": workload_label(args.workload, args.m), "m": args.m, "sample": desc},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 

@@ -31,22 +31,29 @@ def test_algorithmic_bytes():
 def test_recorded_traffic_follows_the_gemm_source_hash(monkeypatch, tmp_path):
     f = tmp_path / "traffic.txt"
     f.write_text(f"# comment: with a colon\ngemm_source_hash: {bench.gemm_source_hash()}\n"
-                 "dram_bytes_per_launch_gate_up: 123456\n")
+                 "dram_bytes_per_launch: 123456\n")
     monkeypatch.setattr(bench, "PROFILE_TRAFFIC", str(f))
     assert bench.recorded_traffic() == 123456.0
-    f.write_text("gemm_source_hash: 0000000000000000\ndram_bytes_per_launch_gate_up: 123456\n")
+    f.write_text("gemm_source_hash: 0000000000000000\ndram_bytes_per_launch: 123456\n")
     assert bench.recorded_traffic() is None                     # taken on another GEMM source
     monkeypatch.setattr(bench, "PROFILE_TRAFFIC", str(tmp_path / "missing.txt"))
     assert bench.recorded_traffic() is None
 
 
-def test_committed_traffic_record_matches_the_current_source():
-    assert bench.recorded_traffic() is not None
+def test_committed_traffic_record_is_readable():
+    """The committed ncu traffic summary names the GEMM source it was taken on
+    and the bytes per launch (bench.py reports it only while that source is
+    current)."""
+    rec = bench.read_traffic_record()
+    assert rec is not None, f"{bench.PROFILE_TRAFFIC} missing or unreadable"
+    assert len(rec[0]) == 16 and rec[1] > 0
 
 
 def test_argument_defaults_and_warmup_floor():
     a = bench.parse_args([])
-    assert (a.gpus, a.steps, a.warmup, a.impl, a.m, a.suite, a.case) == (1, 100, 5, "ours", 8192, False, None)
+    assert (a.gpus, a.steps, a.warmup, a.impl, a.workload, a.m, a.suite, a.case) == \
+        (1, 100, 5, "ours", "qwen", 16384, False, None)
+    assert bench.parse_args(["--workload", "llama"]).m == 8192
     assert bench.parse_args(["--warmup", "1"]).warmup == 3                  # at least 3 warm-up steps
     c = bench.parse_args(["--case", "quant", "--m", "64", "--k", "512", "--bs", "16"])
     assert (c.case, c.m, c.k, c.bs) == ("quant", 64, 512, 16)

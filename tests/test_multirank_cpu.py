@@ -27,7 +27,7 @@ def _worker(rank, world, port, q):
     from nvfp4_quantized_linear_gb300 import synthetic as syn
     local_time = 0.010 * (rank + 1)                    # rank 1 is the slow one
     slowest = bench.max_over_ranks(local_time, "cpu")
-    probs = bench.layer_problems(16, rank)
+    probs = bench.layer_problems(bench.DEFAULT_WORKLOAD, 16, rank)
     x = syn.make_activation(probs[0])
     w = syn.bf16_normal((probs[0].n, probs[0].k), 0.02, probs[0].seed + 100_000)
     seeds = [p.seed for p in probs]
@@ -59,7 +59,7 @@ def test_two_gloo_ranks_shard_batches_and_take_slowest_time():
     assert set(seeds_a).isdisjoint(seeds_b)        # distinct per-rank batches
     assert xa != xb
     import bench
-    flops = sum(p.flops for p in bench.layer_problems(16, 0))
+    flops = sum(p.flops for p in bench.layer_problems(bench.DEFAULT_WORKLOAD, 16, 0))
     assert v0 == v1 == pytest.approx(flops * 2 / 0.020)
 
 
