@@ -183,6 +183,34 @@ size_t nvfp4_mxfp4_scale_bytes(int64_t rows, int64_t k);   /* roundup(rows,128) 
 nvfp4_status nvfp4_mxfp4_quant_act(const void *x_bf16, int64_t m, int64_t k, int64_t ldx,
                                    uint8_t *x_fp4, uint8_t *x_sf, nvfp4_stream_t stream);
 
+/* MXFP4 GEMM, the B12X page's MXFP4 linear backend (mm_mxfp4 on activations
+ * from flashinfer_mxfp4_quantize; section 实现拆解), with the epilogue of
+ * nvfp4_gemm minus alpha (the MX formats have no global scale):
+ *   out[i, j] = bf16( sum_k deq(A)[i,k] * deq(W)[j,k] + bias[j] ),
+ *   deq(q) = e2m1(q) * 2^(code - 127), one E8M0 code per 32 K-elements.
+ *   a_fp4, a_sf     in   activation from nvfp4_mxfp4_quant_act
+ *   w_fp4, w_sf     in   weight [n_w, k] quantized by the same conversion
+ *                        (nvfp4_mxfp4_quant_act applied to the bf16 weight)
+ *   k, n_out, bias_bf16, out_bf16, ldo   as for nvfp4_gemm
+ * The operands' scales use the tiled layout with one column per 32
+ * elements (nvfp4_mxfp4_scale_bytes). */
+nvfp4_status nvfp4_mxfp4_gemm(const uint8_t *a_fp4, const uint8_t *a_sf, int64_t m,
+                              const uint8_t *w_fp4, const uint8_t *w_sf, int64_t n_w, int64_t n_out,
+                              int64_t k, const void *bias_bf16, void *out_bf16, int64_t ldo,
+                              nvfp4_stream_t stream);
+
+/* The whole MXFP4 linear (the B12X page's MXFP4 backend apply path):
+ * nvfp4_mxfp4_quant_act of x into `workspace`, then nvfp4_mxfp4_gemm, on one
+ * stream.  workspace: caller-owned device scratch of at least
+ * align256(nvfp4_packed_bytes(m,k)) + align256(nvfp4_mxfp4_scale_bytes(m,k))
+ * bytes; with nvfp4_mxfp4_linear_workspace_bytes and m <= 128 the GEMM may
+ * split K as nvfp4_linear does. */
+size_t nvfp4_mxfp4_linear_workspace_bytes(int64_t m, int64_t k, int64_t n_w);
+nvfp4_status nvfp4_mxfp4_linear(const void *x_bf16, int64_t m, int64_t k, int64_t ldx,
+                                const uint8_t *w_fp4, const uint8_t *w_sf, int64_t n_w, int64_t n_out,
+                                const void *bias_bf16, void *out_bf16, int64_t ldo,
+                                void *workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
 /* Dynamic activation global scale: the per-tensor AbsMax statistic of the
  * transform page's fusedQuantizeNv computed on the device, for activations
  * without a calibrated scale (the torch-backend page's input_global_scale_inv

@@ -23,6 +23,7 @@ __all__ = [
     "nvfp4_abi_version", "nvfp4_is_supported", "nvfp4_last_error_string", "nvfp4_device_error",
     "nvfp4_packed_bytes", "nvfp4_scale_bytes", "nvfp4_linear_workspace_bytes",
     "nvfp4_prepare_weight", "nvfp4_quant_act", "nvfp4_quant_act_export_y", "nvfp4_act_global_scale", "nvfp4_mxfp4_scale_bytes", "nvfp4_mxfp4_quant_act",
+    "nvfp4_mxfp4_gemm", "nvfp4_mxfp4_linear_workspace_bytes", "nvfp4_mxfp4_linear", "mxfp4_linear",
     "nvfp4_gemm", "nvfp4_gemm_ex", "nvfp4_linear", "nvfp4_linear_noalloc",
     "padded_k", "scale_shape", "quant_act", "quant_act_mx", "prepare_weight", "linear", "act_global_scale",
 ]
@@ -53,6 +54,9 @@ EXPORTS = [
     ("nvfp4_act_global_scale", _I32, [_P, _I64, _I64, _I64, _P, _I32, _P, _P, _P, _P]),
     ("nvfp4_mxfp4_scale_bytes", _SZ, [_I64, _I64]),
     ("nvfp4_mxfp4_quant_act", _I32, [_P, _I64, _I64, _I64, _P, _P, _P]),
+    ("nvfp4_mxfp4_gemm", _I32, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _P, _I64, _P]),
+    ("nvfp4_mxfp4_linear_workspace_bytes", _SZ, [_I64, _I64, _I64]),
+    ("nvfp4_mxfp4_linear", _I32, [_P, _I64, _I64, _I64, _P, _P, _I64, _I64, _P, _P, _I64, _P, _SZ, _P]),
     ("nvfp4_gemm", _I32, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _P, _P, _I64, _P]),
     ("nvfp4_gemm_ex", _I32, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _P, _P, _I64, _I32, ctypes.c_uint64, _I32,
                              _P]),
@@ -199,6 +203,22 @@ def nvfp4_mxfp4_quant_act(x, m: int, k: int, ldx: int, x_fp4, x_sf, stream=None)
     _check(load_library().nvfp4_mxfp4_quant_act(_ptr(x), m, k, ldx, _ptr(x_fp4), _ptr(x_sf), _stream(stream)))
 
 
+def nvfp4_mxfp4_gemm(a_fp4, a_sf, m: int, w_fp4, w_sf, n_w: int, n_out: int, k: int, bias, out, ldo: int,
+                     stream=None) -> None:
+    _check(load_library().nvfp4_mxfp4_gemm(_ptr(a_fp4), _ptr(a_sf), m, _ptr(w_fp4), _ptr(w_sf), n_w, n_out, k,
+                                           _ptr(bias), _ptr(out), ldo, _stream(stream)))
+
+
+def nvfp4_mxfp4_linear_workspace_bytes(m: int, k: int, n_w: int) -> int:
+    return load_library().nvfp4_mxfp4_linear_workspace_bytes(m, k, n_w)
+
+
+def nvfp4_mxfp4_linear(x, m: int, k: int, ldx: int, w_fp4, w_sf, n_w: int, n_out: int, bias, out, ldo: int,
+                       workspace, workspace_bytes: int, stream=None) -> None:
+    _check(load_library().nvfp4_mxfp4_linear(_ptr(x), m, k, ldx, _ptr(w_fp4), _ptr(w_sf), n_w, n_out, _ptr(bias),
+                                             _ptr(out), ldo, _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
 def nvfp4_gemm(a_fp4, a_sf, m: int, w_fp4, w_sf, n_w: int, n_out: int, k: int, alpha, bias, out, ldo: int,
                stream=None) -> None:
     _check(load_library().nvfp4_gemm(_ptr(a_fp4), _ptr(a_sf), m, _ptr(w_fp4), _ptr(w_sf), n_w, n_out, k,
@@ -263,6 +283,22 @@ def quant_act_mx(x, stream=None):
     x_sf = torch.empty(max(nvfp4_mxfp4_scale_bytes(m, k), 1), dtype=torch.uint8, device=x.device)
     nvfp4_mxfp4_quant_act(x, m, k, _ld(x, "x"), x_fp4, x_sf, stream)
     return x_fp4, x_sf
+
+
+def mxfp4_linear(x, w_fp4, w_sf, k: int, n_out: int, bias=None, out=None, workspace=None, stream=None):
+    """out[m, n_out] = MXFP4 linear of a [m, k] bf16 CUDA tensor against a weight
+    quantized by quant_act_mx (allocates out/workspace if not given)."""
+    import torch
+    m = x.shape[0]
+    n_w = w_fp4.shape[0]
+    if out is None:
+        out = torch.empty((m, n_out), dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(max(nvfp4_mxfp4_linear_workspace_bytes(m, k, n_w), 1), dtype=torch.uint8,
+                                device=x.device)
+    nvfp4_mxfp4_linear(x, m, k, _ld(x, "x"), w_fp4, w_sf, n_w, n_out, bias, out, _ld(out, "out"), workspace,
+                       workspace.numel(), stream)
+    return out
 
 
 def prepare_weight(w, w_gs, stream=None):

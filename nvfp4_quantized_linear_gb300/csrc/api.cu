@@ -199,7 +199,7 @@ nvfp4_status check_gemm_args(const uint8_t *a, const uint8_t *a_sf, int64_t m, c
         return fail(NVFP4_ERR_INVALID_ARG, "n_out must satisfy 1 <= n_out <= n_w (got %lld, n_w %lld)", (long long)n_out, (long long)n_w);
     if (ldo < n_out) return fail(NVFP4_ERR_INVALID_ARG, "ldo (%lld) < n_out (%lld)", (long long)ldo, (long long)n_out);
     if (m == 0) return NVFP4_OK;
-    if (!w || !w_sf || !alpha || !out) return fail(NVFP4_ERR_INVALID_ARG, "null pointer argument");
+    if (!w || !w_sf || !out) return fail(NVFP4_ERR_INVALID_ARG, "null pointer argument");
     if (!aligned16(w) || !aligned16(w_sf)) return fail(NVFP4_ERR_ALIGNMENT, "weight buffers must be 16-byte aligned");
     if (!aligned16(out) || (ldo % 8) != 0)
         return fail(NVFP4_ERR_ALIGNMENT, "output rows must start on 16-byte boundaries (pointer and ldo %% 8 == 0)");
@@ -211,17 +211,26 @@ nvfp4_status check_gemm_args(const uint8_t *a, const uint8_t *a_sf, int64_t m, c
     return NVFP4_OK;
 }
 
+// Scale columns (padded to 4) of an operand with logical K = k: NVFP4 has one
+// per 16 elements of the padded K, MXFP4 one per 32.
+int64_t scale_cols_of(int64_t k, bool mx)
+{
+    return mx ? (nvfp4::padded_k(k) / 32 + 3) / 4 * 4 : nvfp4::scale_cols_padded(k);
+}
+
 nvfp4::GemmParams gemm_params(const uint8_t *a_sf, int64_t m, const uint8_t *w_sf, int64_t n_w, int64_t n_out,
                               int64_t k, const float *alpha, const void *bias, void *out, int64_t ldo,
-                              unsigned int *err)
+                              unsigned int *err, bool mx = false)
 {
     nvfp4::GemmParams g;
     g.m = (int32_t)m;
     g.n_w = (int32_t)n_w;
     g.n_out = (int32_t)n_out;
     g.kp = (int32_t)nvfp4::padded_k(k);
-    const int64_t nbp = nvfp4::scale_cols_padded(k);
-    g.num_k64 = (int32_t)(nbp / 4);
+    const int64_t nbp = scale_cols_of(k, mx);
+    g.num_k64 = (int32_t)((g.kp + 63) / 64);
+    g.sf_tiles = (int32_t)(nbp / 4);
+    g.mx = mx ? 1 : 0;
     g.num_m_blk = (int32_t)((m + 127) / 128);
     g.num_n_blk = (int32_t)((n_out + 255) / 256);
     g.sfa = a_sf;
@@ -303,12 +312,13 @@ enum GemmKernel { kGemmAuto = 0, kGemmOneCta = 1, kGemmPair = 2 };
 nvfp4_status run_gemm(const uint8_t *a, const uint8_t *a_sf, int64_t m, const uint8_t *w, const uint8_t *w_sf,
                       int64_t n_w, int64_t n_out, int64_t k, const float *alpha, const void *bias, void *out,
                       int64_t ldo, int num_sms, cudaStream_t s, float *partials = nullptr, size_t partial_bytes = 0,
-                      bool after_quant = false, int kernel = kGemmAuto, uint64_t wait_ns = 0, int drill = 0)
+                      bool after_quant = false, int kernel = kGemmAuto, uint64_t wait_ns = 0, int drill = 0,
+                      bool mx = false)
 {
     unsigned int *err = nullptr;
     cudaError_t e = nvfp4::device_error_word(&err);
     if (e != cudaSuccess) return launch_status(e, "GEMM (error word)");
-    nvfp4::GemmParams g = gemm_params(a_sf, m, w_sf, n_w, n_out, k, alpha, bias, out, ldo, err);
+    nvfp4::GemmParams g = gemm_params(a_sf, m, w_sf, n_w, n_out, k, alpha, bias, out, ldo, err, mx);
     if (wait_ns != 0) g.wait_ns = wait_ns;
     g.drill = drill;
     if (partials != nullptr) {
@@ -334,6 +344,13 @@ nvfp4_status run_gemm(const uint8_t *a, const uint8_t *a_sf, int64_t m, const ui
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
 }  // namespace
+
+// Smallest workspace of nvfp4_mxfp4_linear: the MXFP4 activation and its scales.
+static size_t mx_min_workspace_bytes(int64_t m, int64_t k)
+{
+    if (m <= 0 || k <= 0) return 0;
+    return align256(nvfp4_packed_bytes(m, k)) + align256(nvfp4_mxfp4_scale_bytes(m, k));
+}
 
 size_t nvfp4::linear_min_workspace_bytes(int64_t m, int64_t k)
 {
@@ -538,7 +555,7 @@ nvfp4_status nvfp4_gemm_ex(const uint8_t *a_fp4, const uint8_t *a_sf, int64_t m,
                                       alpha_dev, bias_bf16, out_bf16, ldo);
     if (st != NVFP4_OK) return st;
     if (m == 0) return ok();
-    if (!a_fp4 || !a_sf) return fail(NVFP4_ERR_INVALID_ARG, "null pointer argument");
+    if (!a_fp4 || !a_sf || !alpha_dev) return fail(NVFP4_ERR_INVALID_ARG, "null pointer argument");
     Range outs[1] = {range2d(out_bf16, m, n_out, ldo, "out")};
     Range ins[6] = {range(a_fp4, nvfp4_packed_bytes(m, k), "a_fp4"), range(a_sf, nvfp4_scale_bytes(m, k), "a_sf"),
                     range(w_fp4, nvfp4_packed_bytes(n_w, k), "w_fp4"), range(w_sf, nvfp4_scale_bytes(n_w, k), "w_sf"),
@@ -575,6 +592,7 @@ nvfp4_status nvfp4_linear(const void *x_bf16, int64_t m, int64_t k, int64_t ldx,
     st = check_gemm_args(nullptr, nullptr, m, w_fp4, w_sf, n_w, n_out, k, alpha_dev, bias_bf16, out_bf16, ldo);
     if (st != NVFP4_OK) return st;
     if (m == 0) return ok();
+    if (!alpha_dev) return fail(NVFP4_ERR_INVALID_ARG, "null pointer argument");
     if (workspace_bytes < need)
         return fail(NVFP4_ERR_WORKSPACE, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, need);
     Range outs[2] = {range2d(out_bf16, m, n_out, ldo, "out"), range(workspace, workspace_bytes, "workspace")};
@@ -592,6 +610,73 @@ nvfp4_status nvfp4_linear(const void *x_bf16, int64_t m, int64_t k, int64_t ldx,
     float *partials = workspace_bytes > need ? reinterpret_cast<float *>(ws + need) : nullptr;
     return run_gemm(a_fp4, a_sf, m, w_fp4, w_sf, n_w, n_out, k, alpha_dev, bias_bf16, out_bf16, ldo, num_sms, s,
                     partials, workspace_bytes > need ? workspace_bytes - need : 0, true);
+}
+
+size_t nvfp4_mxfp4_linear_workspace_bytes(int64_t m, int64_t k, int64_t n_w)
+{
+    (void)n_w;
+    if (m <= 0 || k <= 0) return 0;
+    const size_t base = mx_min_workspace_bytes(m, k);
+    return m <= 128 ? base + align256(kSplitBytesPerRow * (size_t)m) : base;
+}
+
+nvfp4_status nvfp4_mxfp4_gemm(const uint8_t *a_fp4, const uint8_t *a_sf, int64_t m, const uint8_t *w_fp4,
+                              const uint8_t *w_sf, int64_t n_w, int64_t n_out, int64_t k, const void *bias_bf16,
+                              void *out_bf16, int64_t ldo, nvfp4_stream_t stream)
+{
+    nvfp4_status st = check_gemm_args(m > 0 ? a_fp4 : nullptr, m > 0 ? a_sf : nullptr, m, w_fp4, w_sf, n_w, n_out, k,
+                                      nullptr, bias_bf16, out_bf16, ldo);
+    if (st != NVFP4_OK) return st;
+    if (m == 0) return ok();
+    if (!a_fp4 || !a_sf) return fail(NVFP4_ERR_INVALID_ARG, "null pointer argument");
+    Range outs[1] = {range2d(out_bf16, m, n_out, ldo, "out")};
+    Range ins[5] = {range(a_fp4, nvfp4_packed_bytes(m, k), "a_fp4"), range(a_sf, nvfp4_mxfp4_scale_bytes(m, k), "a_sf"),
+                    range(w_fp4, nvfp4_packed_bytes(n_w, k), "w_fp4"),
+                    range(w_sf, nvfp4_mxfp4_scale_bytes(n_w, k), "w_sf"),
+                    range(bias_bf16, bias_bf16 ? (size_t)n_out * 2 : 0, "bias")};
+    if ((st = check_aliases(outs, 1, ins, 5)) != NVFP4_OK) return st;
+    int num_sms = 0;
+    if ((st = current_device(&num_sms)) != NVFP4_OK) return st;
+    return run_gemm(a_fp4, a_sf, m, w_fp4, w_sf, n_w, n_out, k, nullptr, bias_bf16, out_bf16, ldo, num_sms,
+                    reinterpret_cast<cudaStream_t>(stream), nullptr, 0, false, kGemmAuto, 0, 0, true);
+}
+
+nvfp4_status nvfp4_mxfp4_linear(const void *x_bf16, int64_t m, int64_t k, int64_t ldx, const uint8_t *w_fp4,
+                                const uint8_t *w_sf, int64_t n_w, int64_t n_out, const void *bias_bf16,
+                                void *out_bf16, int64_t ldo, void *workspace, size_t workspace_bytes,
+                                nvfp4_stream_t stream)
+{
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const size_t need = mx_min_workspace_bytes(m, k);           // MXFP4 activation + scales
+    uint8_t *a_fp4 = ws;
+    uint8_t *a_sf = ws ? ws + align256(nvfp4_packed_bytes(m, k)) : nullptr;
+    // the quantizer's checks, with a_sf standing in for the (absent) global scale
+    nvfp4_status st = check_quant_args(x_bf16, m, k, ldx, reinterpret_cast<const float *>(a_sf), nullptr, 0,
+                                       m > 0 ? a_fp4 : nullptr, m > 0 ? a_sf : nullptr, "x");
+    if (st == NVFP4_ERR_INVALID_ARG && m > 0 && workspace == nullptr)
+        return fail(NVFP4_ERR_WORKSPACE, "workspace is NULL (need %zu bytes)", need);
+    if (st != NVFP4_OK) return st;
+    st = check_gemm_args(nullptr, nullptr, m, w_fp4, w_sf, n_w, n_out, k, nullptr, bias_bf16, out_bf16, ldo);
+    if (st != NVFP4_OK) return st;
+    if (m == 0) return ok();
+    if (workspace_bytes < need)
+        return fail(NVFP4_ERR_WORKSPACE, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, need);
+    Range outs[2] = {range2d(out_bf16, m, n_out, ldo, "out"), range(workspace, workspace_bytes, "workspace")};
+    Range ins[4] = {range2d(x_bf16, m, k, ldx, "x"), range(w_fp4, nvfp4_packed_bytes(n_w, k), "w_fp4"),
+                    range(w_sf, nvfp4_mxfp4_scale_bytes(n_w, k), "w_sf"),
+                    range(bias_bf16, bias_bf16 ? (size_t)n_out * 2 : 0, "bias")};
+    if ((st = check_aliases(outs, 2, ins, 4)) != NVFP4_OK) return st;
+    int num_sms = 0;
+    if ((st = current_device(&num_sms)) != NVFP4_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    nvfp4::QuantParams p = quant_params(x_bf16, m, k, ldx, nullptr, nullptr, 0, a_fp4, a_sf);
+    p.nb = (int32_t)(nvfp4::padded_k(k) / 32);
+    p.nbp = (p.nb + 3) / 4 * 4;
+    st = launch_status(nvfp4::launch_quant_mx(p, num_sms, s), "MXFP4 quantize kernel");
+    if (st != NVFP4_OK) return st;
+    float *partials = workspace_bytes > need ? reinterpret_cast<float *>(ws + need) : nullptr;
+    return run_gemm(a_fp4, a_sf, m, w_fp4, w_sf, n_w, n_out, k, nullptr, bias_bf16, out_bf16, ldo, num_sms, s,
+                    partials, workspace_bytes > need ? workspace_bytes - need : 0, true, kGemmAuto, 0, 0, true);
 }
 
 }  // extern "C"

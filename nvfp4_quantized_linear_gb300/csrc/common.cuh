@@ -45,12 +45,14 @@ constexpr int kMaxSplits = 16;       // split-K ranges at most
 
 struct GemmParams {
     int32_t m, n_w, n_out, kp;
-    int32_t num_k64;                 // kp / 64 rounded up (= scale_cols_padded / 4)
+    int32_t num_k64;                 // kp / 64 rounded up: K-steps of the MMA
+    int32_t sf_tiles;                // 512-byte scale tiles per 128-row band (scale columns / 4)
+    int32_t mx;                      // 1: MXFP4 operands (UE8M0 scales per 32 elements, no alpha)
     int32_t num_m_blk, num_n_blk;
     const uint8_t *sfa, *sfb;        // tiled scales
     int64_t sfa_band_bytes;          // bytes per 128-row band of scales
     int64_t sfb_band_bytes;
-    const float *alpha;
+    const float *alpha;              // device fp32; nullptr reads as 1 (MXFP4)
     const uint16_t *bias;            // bf16 bits or nullptr
     uint16_t *out;                   // bf16 bits
     int64_t ldo;

@@ -102,6 +102,10 @@ __device__ __forceinline__ Work work_of(int item, const GemmParams &p, int num_k
     return w;
 }
 
+// kMx: MXFP4 operands (one UE8M0 scale per 32 K-elements, two 512-byte scale
+// tiles per band and stage, scale_vec::2X MMAs); otherwise NVFP4 (one UE4M3
+// scale per 16 K-elements, four tiles per band and stage, scale_vec::4X).
+template <bool kMx>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmOut, const GemmParams p)
@@ -167,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t acc = tmem + ((uint32_t)(q * 32) << 16) + hcol;
         const uint32_t out_stage = smem_u32(smem + kOffOut) + (warp - kEpiWarp0) * kOutChunkBytes;
         const bool use_bias = p.splits == 1 && p.bias != nullptr;
-        const float alpha = __ldg(p.alpha);
+        const float alpha = p.alpha != nullptr ? __ldg(p.alpha) : 1.0f;
         const uint64_t out_policy = l2_policy_evict_first();   // the output is written once
         uint32_t acc_phase = 0;
         int it = 0;
@@ -288,24 +292,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int ks = wk.ks0; ks < wk.ks1; ++ks) {
                 ok = __all_sync(~0u, mbar_wait(&full[stage], phase, p.err_flag, kErrTimeout, p.wait_ns));
                 if (!ok) break;
-                uint32_t a[16], b[32];
+                constexpr int kT = kSfTilesPerStage<kMx>;
+                uint32_t a[4 * kT], b[8 * kT];
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint4 v = ld_shared_v4(sfa_smem + stage * kSfaBytes + kk * 512);
-                    a[kk * 4 + 0] = v.x; a[kk * 4 + 1] = v.y; a[kk * 4 + 2] = v.z; a[kk * 4 + 3] = v.w;
+                for (int j = 0; j < kT; ++j) {
+                    const uint4 v = ld_shared_v4(sfa_smem + stage * kSfaBytes + j * 512);
+                    a[j * 4 + 0] = v.x; a[j * 4 + 1] = v.y; a[j * 4 + 2] = v.z; a[j * 4 + 3] = v.w;
                 }
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
+                for (int j = 0; j < kT; ++j)
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        const uint4 v = ld_shared_v4(sfb_smem + stage * kSfbBytes + h * 2048 + kk * 512);
-                        uint32_t *d = b + kk * 8 + h * 4;
+                        const uint4 v = ld_shared_v4(sfb_smem + stage * kSfbBytes + h * 2048 + j * 512);
+                        uint32_t *d = b + j * 8 + h * 4;
                         d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
                     }
                 // (tiles past the valid K-steps or B rows hold stale bytes; the
                 // MMAs never read their columns)
-                tmem_st_16cols(sf_tmem + stage * kSfColsPerStage, a);
-                tmem_st_32cols(sf_tmem + stage * kSfColsPerStage + 16, b);
+                if constexpr (kMx) {
+                    tmem_st_8cols(sf_tmem + stage * kSfColsPerStage, a);
+                    tmem_st_16cols(sf_tmem + stage * kSfColsPerStage + 4 * kT, b);
+                } else {
+                    tmem_st_16cols(sf_tmem + stage * kSfColsPerStage, a);
+                    tmem_st_32cols(sf_tmem + stage * kSfColsPerStage + 4 * kT, b);
+                }
                 tmem_st_wait();
                 tc_fence_before_sync();
                 __syncwarp();
@@ -340,18 +350,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int halves = min(kBN, p.n_out - t.nb * kBN) > 128 ? 2 : 1;
                 for (int ks = wk.ks0; ks < wk.ks1; ++ks) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, p.err_flag, kErrTimeout, p.wait_ns)) { ok = false; break; }
-                    const uint32_t sf_bytes = (uint32_t)min(4, p.num_k64 - ks * 4) * 512;
+                    constexpr int kT = kSfTilesPerStage<kMx>;
+                    const uint32_t sf_bytes = (uint32_t)min(kT, p.sf_tiles - ks * kT) * 512;
                     if (act_side) {
                         mbar_arrive_expect_tx(&full[stage], kABytes + sf_bytes);
                         tma_load_2d(smem + kOffA + stage * kABytes, &tmA, &full[stage], ks * kBKBytes, t.mb * kBM, pol);
                         bulk_load(smem + kOffSfa + stage * kSfaBytes,
-                                  p.sfa + t.mb * p.sfa_band_bytes + (int64_t)ks * 2048, sf_bytes, &full[stage], pol);
+                                  p.sfa + t.mb * p.sfa_band_bytes + (int64_t)ks * kT * 512, sf_bytes, &full[stage], pol);
                     } else {
                         mbar_arrive_expect_tx(&full[stage], kBBytes + sf_bytes * halves);
                         tma_load_2d(smem + kOffB + stage * kBBytes, &tmB, &full[stage], ks * kBKBytes, t.nb * kBN, pol);
                         for (int h = 0; h < halves; ++h)    // halves == 2 implies band t.nb*2+1 exists
                             bulk_load(smem + kOffSfb + stage * kSfbBytes + h * 2048,
-                                      p.sfb + (t.nb * 2 + h) * p.sfb_band_bytes + (int64_t)ks * 2048, sf_bytes,
+                                      p.sfb + (t.nb * 2 + h) * p.sfb_band_bytes + (int64_t)ks * kT * 512, sf_bytes,
                                       &full[stage], pol);
                     }
                     issued_mask |= 1u << stage;
@@ -396,7 +407,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
                 const Work wk = work_of(tile, p, num_ks);
                 const int n_rows = min(kBN, p.n_out - wk.t.nb * kBN);
-                const uint32_t idesc = n_rows > 128 ? idesc_nvf4(128, 256) : idesc_nvf4(128, 128);
+                const uint32_t n_mma = n_rows > 128 ? 256 : 128;
+                const uint32_t idesc = idesc_nvf4(128, n_mma);
                 if (!__all_sync(~0u, mbar_wait(tmem_empty, acc_phase ^ 1, p.err_flag, kErrTimeout, p.wait_ns))) break;
                 tc_fence_after_sync();
                 for (int ks = wk.ks0; ks < wk.ks1; ++ks) {
@@ -414,8 +426,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (leader) {
                         for (int kk = 0; kk < kcount; ++kk) {
                             // K-step kk starts 32 bytes further into the swizzled 128-byte rows
-                            tc_mma_nvf4(tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc,
-                                        sf_col + kk * 4, sf_col + 16 + kk * 8, (ks != wk.ks0 || kk != 0));
+                            const uint64_t ad = adesc + (uint64_t)(kk * 2), bd = bdesc + (uint64_t)(kk * 2);
+                            const uint32_t acc_flag = (ks != wk.ks0 || kk != 0);
+                            if constexpr (kMx)      // two UE8M0 scales per row and K-step: half a scale word
+                                tc_mma_mxf4(tmem, ad, bd, idesc_mxf4(128, n_mma, (kk & 1) * 2),
+                                            sf_col + (kk >> 1) * 4, sf_col + 8 + (kk >> 1) * 8, acc_flag);
+                            else
+                                tc_mma_nvf4(tmem, ad, bd, idesc, sf_col + kk * 4, sf_col + 16 + kk * 8, acc_flag);
                         }
                         tc_commit(&empty[stage]);
                     }
@@ -445,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const GemmParams p)
 {
     griddep_wait();                                 // the split GEMM's partials are complete
-    const float alpha = __ldg(p.alpha);
+    const float alpha = p.alpha != nullptr ? __ldg(p.alpha) : 1.0f;
     const int groups = (p.n_out + 3) / 4;
     const int64_t total = (int64_t)p.m * groups;
     const int64_t split_stride = (int64_t)p.m * p.part_ld;
@@ -502,8 +519,11 @@ cudaError_t launch_gemm(const GemmParams &p, const uint8_t *a, const uint8_t *w,
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
-        cudaError_t e =
-            cudaFuncSetAttribute(gemm_nvf4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(gemm_nvf4_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gemm_nvf4_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kSmemBytes);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
@@ -534,7 +554,8 @@ cudaError_t launch_gemm(const GemmParams &p, const uint8_t *a, const uint8_t *w,
     cfg.stream = s;
     cfg.attrs = dependent ? &attr : nullptr;
     cfg.numAttrs = dependent ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gemm_nvf4_kernel, tmA, tmB, tmOut, p);
+    return p.mx ? cudaLaunchKernelEx(&cfg, gemm_nvf4_kernel<true>, tmA, tmB, tmOut, p)
+                : cudaLaunchKernelEx(&cfg, gemm_nvf4_kernel<false>, tmA, tmB, tmOut, p);
 }
 
 }  // namespace nvfp4

@@ -14,6 +14,12 @@ struct Tile {
     int mb, nb;
 };
 
+// 512-byte scale tiles (128 rows x 4 scale columns) per 128-row band in one
+// 256-element K stage: NVFP4 has a scale per 16 elements (4 tiles), MXFP4 one
+// per 32 (2 tiles).
+template <bool kMx>
+constexpr int kSfTilesPerStage = kMx ? 2 : 4;
+
 // Tiles are walked column by column (row band fastest) inside groups of up to
 // 64 row bands: the CTAs resident at one time work on a few weight column
 // bands, so each weight tile is streamed from DRAM about once and shared by
@@ -81,6 +87,42 @@ inline bool make_output_map(CUtensorMap *map, void *base, uint64_t n_out, uint64
     cuuint32_t estr[2] = {1, 1};
     return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base, dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Map of the bf16 output [m, n_out] (row stride ldo elements) for TMA stores
+// of 64-column x 32-row boxes (128-byte rows) with the 128-byte swizzle; the
+// TMA skips elements outside [0, n_out) x [0, m).  Requires a 16-B aligned base
+// and ldo % 8 == 0.
+inline bool make_output_map_sw128(CUtensorMap *map, void *base, uint64_t n_out, uint64_t m, uint64_t ldo)
+{
+    auto encode = tensor_map_encoder();
+    if (encode == nullptr) return false;
+    cuuint64_t dims[2] = {n_out, m};
+    cuuint64_t strides[1] = {ldo * 2};
+    cuuint32_t box[2] = {64, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Map of a tiled scale tensor viewed as [bands, band_bytes / 8] 8-byte
+// elements (one row per 128-row band), for copies of `box_elems` elements of
+// two consecutive bands at once (the scale tiles of one K stage of a 256-row
+// operand tile); zero fill past the last band or the band's end.  band_bytes
+// is a multiple of 512 and the base 16-B aligned.
+inline bool make_scale_bands_map(CUtensorMap *map, const void *base, uint64_t band_bytes, uint64_t bands,
+                                 uint32_t box_elems)
+{
+    auto encode = tensor_map_encoder();
+    if (encode == nullptr) return false;
+    cuuint64_t dims[2] = {band_bytes / 8, bands};
+    cuuint64_t strides[1] = {band_bytes};
+    cuuint32_t box[2] = {box_elems, 2};
+    cuuint32_t estr[2] = {1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -235,6 +235,22 @@ __device__ __forceinline__ void tc_mma_nvf4(uint32_t d_tmem, uint64_t a_desc, ui
         : "memory");
 }
 
+// The same with one UE8M0 scale per 32 K-elements (MXFP4, scale_vec::2X): each
+// 32-bit TMEM scale word holds four consecutive block scales of a row, and the
+// instruction descriptor's scale-factor ids (0 or 2) say which two of them this
+// K = 64 step uses.
+__device__ __forceinline__ void tc_mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 // D(tmem) (+)= A(smem) * B(smem)^T with bf16 operands, fp32 accumulation
 // (kind::f16, K = 16).
 __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -280,6 +296,14 @@ __device__ __forceinline__ void tmem_st_16cols(uint32_t taddr, const uint32_t (&
     asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
                  :
                  : "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_8cols(uint32_t taddr, const uint32_t (&r)[8])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 :
+                 : "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
                  : "memory");
 }
 
@@ -399,6 +423,14 @@ __host__ __device__ constexpr uint32_t idesc_nvf4(uint32_t M, uint32_t N)
            | (1u << 10)           // B format: E2M1
            | ((N >> 3) << 17)     // N / 8
            | ((M >> 4) << 24);    // M / 16   (scale format bit 23 = 0: UE4M3; scale ids 0)
+}
+
+// The same for MXFP4 operands: UE8M0 scales (bit 23), scale-factor ids
+// sf_id (0 or 2: the first or second pair of block scales in each scale word)
+// for both A (bits 29-30) and B (bits 4-5).
+__host__ __device__ constexpr uint32_t idesc_mxf4(uint32_t M, uint32_t N, uint32_t sf_id)
+{
+    return idesc_nvf4(M, N) | (1u << 23) | (sf_id << 4) | (sf_id << 29);
 }
 
 // Instruction descriptor of the kind::f16 MMA: bf16 x bf16, fp32 accumulate,
@@ -533,6 +565,19 @@ __device__ __forceinline__ void tc_mma_pair_nvf4(uint32_t d_tmem, uint64_t a_des
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %6, 0;\n\t"
         "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Pair block-scaled MMA with UE8M0 scales per 32 K-elements (MXFP4; see tc_mma_mxf4).
+__device__ __forceinline__ void tc_mma_pair_mxf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
             d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");

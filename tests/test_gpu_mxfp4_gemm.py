@@ -1,0 +1,122 @@
+"""GPU parity of the MXFP4 GEMM and linear (nvfp4_mxfp4_gemm,
+nvfp4_mxfp4_linear) against the oracle's FP64 MXFP4 GEMM (reading R-mx) on
+identical quantized operands, at the GEMM tolerance (max|err| <= 2e-2 rms,
+relative Frobenius error <= 5e-3).
+
+Page "B12X quantized linear backends" (vLLM PR #52016), section 实现拆解:
+the MXFP4 backend quantizes the activation (flashinfer_mxfp4_quantize) and
+runs mm_mxfp4.  Here the weight is quantized by the same conversion, so the
+oracle's operands are its own MXFP4 quantization of the same bf16 inputs
+(which the quantizer tests show to be the library's bytes)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from _helpers import assert_gemm_close, bf16_to_f64, nv, require_library, sample_indices, syn, tile_edges
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    return require_library()
+
+
+def _quant(x):
+    return nv.quant_act_mx(x)
+
+
+def _oracle(x, w, b, k, rows, cols):
+    a, sa = oracle.quantize_mx(syn.bf16_bits(x[torch.from_numpy(rows).to(x.device)].cpu()), k=k)
+    bq, sb = oracle.quantize_mx(syn.bf16_bits(w[torch.from_numpy(cols).to(w.device)].cpu()), k=k)
+    bb = syn.bf16_bits(b[torch.from_numpy(cols).to(b.device)].cpu()) if b is not None else None
+    return oracle.gemm_mx(a, sa, bq, sb, bb)
+
+
+# (m, k, n_w, n_out, bias, x kind): one-CTA (m <= 128) and CTA-pair (m > 128)
+# kernels, ragged K (K % 32 != 0 and K % 64 != 0), output slices, full-size
+# Llama / Qwen layer shapes (sampled rows x columns)
+CASES = [
+    (16, 256, 128, 128, False, "normal"),
+    (1, 4096, 6144, 6144, True, "normal"),
+    (97, 4104, 1024, 1000, True, "outlier"),
+    (128, 5128, 512, 384, False, "student_t"),
+    (300, 96, 640, 640, True, "normal"),
+    (257, 4104, 11008, 10944, True, "normal"),
+    (8192, 4096, 28672, 28672, False, "normal"),
+    (2048, 5120, 10240, 10240, False, "outlier"),
+]
+
+
+@pytest.mark.parametrize("m,k,n_w,n_out,bias,kind", CASES, ids=[f"m{c[0]}-k{c[1]}-n{c[2]}-o{c[3]}" for c in CASES])
+def test_mxfp4_gemm_matches_oracle(m, k, n_w, n_out, bias, kind):
+    seed = 6100 + m + k + n_w
+    if kind == "normal":
+        x = syn.bf16_normal((m, k), 1.0, seed, device="cuda")
+    elif kind == "outlier":
+        x = syn.bf16_outlier_channels(m, k, seed, device="cuda")
+    else:
+        x = syn.bf16_student_t(m, k, 3, seed, device="cuda")
+    w = syn.bf16_normal((n_w, k), 0.02, seed + 1, device="cuda")
+    b = syn.bf16_normal((n_out,), 0.1, seed + 2, device="cuda") if bias else None
+    a_fp4, a_sf = _quant(x)
+    w_fp4, w_sf = _quant(w)
+    ldo = (n_out + 7) // 8 * 8
+    out = torch.full((m, ldo), float("nan"), dtype=torch.bfloat16, device="cuda")
+    nv.nvfp4_mxfp4_gemm(a_fp4, a_sf, m, w_fp4, w_sf, n_w, n_out, k, b, out, ldo)
+    lin = nv.mxfp4_linear(x, w_fp4, w_sf, k, n_out, bias=b)
+    torch.cuda.synchronize()
+    nv.nvfp4_device_error()
+    rows = np.arange(m) if m <= 64 else sample_indices(m, 48, seed, must=tile_edges(m, 128))
+    cols = np.arange(n_out) if n_out <= 384 else sample_indices(n_out, 384, seed + 1, must=tile_edges(n_out, 128))
+    ref = _oracle(x, w, b, k, rows, cols)
+    assert_gemm_close(bf16_to_f64(out[:, :n_out])[rows][:, cols], ref, f"mxfp4 gemm {m}x{k}->{n_out}")
+    assert_gemm_close(bf16_to_f64(lin)[rows][:, cols], ref, f"mxfp4 linear {m}x{k}->{n_out}")
+    assert torch.isnan(out[:, n_out:]).all() if ldo > n_out else True
+
+
+def test_mxfp4_gemm_exact_power_of_two_case_is_bit_exact():
+    """Every element a grid value times a power of two per 32-block: the MXFP4
+    quantization is exact, so the GEMM computes sum_k x w exactly in fp32
+    (small integers) and the bf16 output equals the rounded exact product."""
+    rng = np.random.default_rng(61)
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    m, n, k = 200, 384, 320
+    xa = rng.choice(grid, (m, k)) * rng.choice([-1, 1], (m, k))
+    xw = rng.choice(grid, (n, k)) * rng.choice([-1, 1], (n, k))
+    xa[:, ::32] = 6                                  # every block's maximum is 6: scale 2^0
+    xw[:, ::32] = 6
+    x = torch.tensor(xa, dtype=torch.float32).to(torch.bfloat16).cuda()
+    w = torch.tensor(xw, dtype=torch.float32).to(torch.bfloat16).cuda()
+    a_fp4, a_sf = _quant(x)
+    w_fp4, w_sf = _quant(w)
+    out = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+    nv.nvfp4_mxfp4_gemm(a_fp4, a_sf, m, w_fp4, w_sf, n, n, k, None, out, n)
+    torch.cuda.synchronize()
+    exact = torch.from_numpy(xa @ xw.T)
+    assert (exact.abs() < 2 ** 22).all()
+    assert torch.equal(out.cpu().view(torch.int16), exact.float().to(torch.bfloat16).view(torch.int16))
+
+
+@pytest.mark.parametrize("m,k,n", [(1, 14336, 4096), (64, 4096, 2048)])
+def test_mxfp4_linear_split_k_matches_unsplit(m, k, n):
+    """Small m with the full workspace splits K (fp32 partials + ordered
+    reduce); against the oracle and the unsplit GEMM (minimum workspace)."""
+    x = syn.bf16_normal((m, k), 1.0, 6200 + m, device="cuda")
+    w = syn.bf16_normal((n, k), 0.02, 6201, device="cuda")
+    w_fp4, w_sf = _quant(w)
+    full = nv.nvfp4_mxfp4_linear_workspace_bytes(m, k, n)
+    small = (nv.nvfp4_packed_bytes(m, k) + 255) // 256 * 256 + (nv.nvfp4_mxfp4_scale_bytes(m, k) + 255) // 256 * 256
+    assert full > small
+    outs = []
+    for ws_bytes in (full, small):
+        ws = torch.full((ws_bytes,), 0xA5, dtype=torch.uint8, device="cuda")
+        outs.append(nv.mxfp4_linear(x, w_fp4, w_sf, k, n, workspace=ws))
+    torch.cuda.synchronize()
+    nv.nvfp4_device_error()
+    rows = np.arange(m)
+    cols = sample_indices(n, 384, 6202, must=tile_edges(n, 128))
+    ref = _oracle(x, w, None, k, rows, cols)
+    for o in outs:
+        assert_gemm_close(bf16_to_f64(o)[rows][:, cols], ref, "mxfp4 linear split/unsplit")
