@@ -47,14 +47,14 @@ constexpr uint32_t kABytes = kRowsCta * kBKBytes;     // 16 KB: this CTA's A row
 constexpr uint32_t kBBytes = kRowsCta * kBKBytes;     // 16 KB: this CTA's half of B
 constexpr uint32_t kSfaBytes = 4 * 512;               // this CTA's A band, 4 K-steps
 constexpr uint32_t kSfbBytes = 2 * 4 * 512;           // both B bands of the tile
-constexpr uint32_t kOutChunkBytes = 32 * 16 * 2;      // output staging: 32 rows x 16 columns bf16
+constexpr uint32_t kOutChunkBytes = 32 * 64 * 2;      // output staging: 32 rows x 64 columns bf16 (4 KB)
 constexpr uint32_t kOffA = 0;
 constexpr uint32_t kOffB = kOffA + kStages * kABytes;
 constexpr uint32_t kOffSfa = kOffB + kStages * kBBytes;
 constexpr uint32_t kOffSfb = kOffSfa + kStages * kSfaBytes;
 constexpr uint32_t kOffBias = kOffSfb + kStages * kSfbBytes;  // two tiles of bias (bf16)
-constexpr uint32_t kOffOut = kOffBias + 2 * kTileN * 2;       // per epilogue warp: two staging chunks
-constexpr uint32_t kOffBar = kOffOut + 8 * 2 * kOutChunkBytes;
+constexpr uint32_t kOffOut = (kOffBias + 2 * kTileN * 2 + 1023) / 1024 * 1024;   // one chunk per epilogue warp
+constexpr uint32_t kOffBar = kOffOut + 8 * kOutChunkBytes;
 constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;         // barriers + alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemSf = 256;
@@ -68,13 +68,16 @@ constexpr uint16_t kBothCtas = 0x3;
 constexpr uint32_t kRegsCtl = 56, kRegsSf = 96, kRegsEpi = 176;
 
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kOffOut % 128 == 0, "TMA store sources are 128-byte aligned");
+static_assert(kOffOut % 1024 == 0, "128-byte-swizzled TMA store sources are 1024-byte aligned");
 static_assert(kTmemSf + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
 static_assert(128 * (kRegsCtl + kRegsSf + 2 * kRegsEpi) <= kThreads * 128, "register reallocation budget");
 
+// kMx: MXFP4 operands (UE8M0 scales per 32 K-elements, scale_vec::2X), else NVFP4.
+template <bool kMx>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_nvf4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                          const __grid_constant__ CUtensorMap tmOut, const GemmParams p)
+                          const __grid_constant__ CUtensorMap tmSfb, const __grid_constant__ CUtensorMap tmOut,
+                          const GemmParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -109,6 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbarrier_init();
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
+        prefetch_tensormap(&tmSfb);
     }
     if (warp == 1) {
         tmem_alloc_pair(tmem_slot, kTmemCols);
@@ -132,10 +136,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;
         const int hcol = ((warp - kEpiWarp0) >> 2) * kEpiCols;
         const uint32_t acc = tmem + ((uint32_t)(q * 32) << 16) + hcol;
-        const uint32_t out_stage = smem_u32(smem + kOffOut) + (warp - kEpiWarp0) * 2 * kOutChunkBytes;
+        const uint32_t out_stage = smem_u32(smem + kOffOut) + (warp - kEpiWarp0) * kOutChunkBytes;
         const uint32_t leader_tmem_empty = mapa_shared(tmem_empty, 0);
         const bool use_bias = p.bias != nullptr;
-        const float alpha = __ldg(p.alpha);
+        const float alpha = p.alpha != nullptr ? __ldg(p.alpha) : 1.0f;
         const uint64_t out_policy = l2_policy_evict_first();   // the output is written once
         uint32_t acc_phase = 0;
         int it = 0;
@@ -151,6 +155,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after_sync();
             acc_phase ^= 1;
 
+            // Drain this warp's 128 accumulator columns in four 32-column
+            // loads, double-buffered: the next load is in flight while the
+            // current chunk gets alpha and bias and is rounded.  The
+            // accumulator goes back to the MMA warp right after the last load
+            // has landed, before that chunk's arithmetic.
             uint32_t r0[32], r1[32];
             uint32_t packed[kEpiCols / 2];
             if (n_cols > 0) tmem_ld_32cols(acc, r0);
@@ -158,9 +167,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int ch = 0; ch < kEpiCols / 32; ++ch) {
                 uint32_t(&cur)[32] = (ch & 1) ? r1 : r0;
                 uint32_t(&nxt)[32] = (ch & 1) ? r0 : r1;
-                if (ch * 32 < n_cols) {                         // uniform across the warp
+                if (n_cols > 0) {                               // uniform across the warp
                     tmem_ld_wait_regs(cur);
-                    if (ch + 1 < kEpiCols / 32 && (ch + 1) * 32 < n_cols) tmem_ld_32cols(acc + (ch + 1) * 32, nxt);
+                    if (ch + 1 < kEpiCols / 32) tmem_ld_32cols(acc + (ch + 1) * 32, nxt);
+                }
+                if (ch + 1 == kEpiCols / 32) {
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (is_leader) mbar_arrive(tmem_empty);  // the leader's own barrier: local arrive
+                        else mbar_arrive_remote(leader_tmem_empty);
+                    }
+                }
+                if (ch * 32 < n_cols) {                         // uniform across the warp
 #pragma unroll
                     for (int j = 0; j < 32; j += 2) {
                         float b0 = 0.0f, b1 = 0.0f;
@@ -174,31 +193,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) {
-                if (is_leader) mbar_arrive(tmem_empty);          // the leader's own barrier: local arrive
-                else mbar_arrive_remote(leader_tmem_empty);
-                if (use_bias) mbar_arrive(&bias_empty[it & 1]);
+            if (use_bias) {
+                __syncwarp();                                   // every lane has read the bias buffer
+                if (lane == 0) mbar_arrive(&bias_empty[it & 1]);
             }
 
-            // TMA stores of 16-column chunks through two staging buffers; rows
-            // >= m and columns >= n_out are clipped by the TMA.
+            // TMA stores of two 32-row x 64-column chunks (128-byte rows, the
+            // TMA's 128-byte swizzle: 16-byte piece j of row r sits at piece
+            // j ^ (r % 8), which also spreads the 32 lanes' writes over all
+            // banks) through this warp's staging buffer; rows >= m and
+            // columns >= n_out are clipped by the TMA.
             const int row0 = t.mb * kTileM + (int)rank * kRowsCta + q * 32;
 #pragma unroll
-            for (int c = 0; c < kEpiCols / 16; ++c) {
-                if (c * 16 < n_cols) {                          // uniform across the warp
-                    const uint32_t buf = out_stage + (c & 1) * kOutChunkBytes;
-                    if (lane == 0) bulk_wait_group_read<1>();   // the store that last read `buf` is done with it
+            for (int c = 0; c < kEpiCols / 64; ++c) {
+                if (c * 64 < n_cols) {                          // uniform across the warp
+                    if (lane == 0) bulk_wait_group_read<0>();   // the previous store has read the buffer
                     __syncwarp();
-                    st_shared_v4(buf + lane * 32, packed[c * 8], packed[c * 8 + 1], packed[c * 8 + 2],
-                                 packed[c * 8 + 3]);
-                    st_shared_v4(buf + lane * 32 + 16, packed[c * 8 + 4], packed[c * 8 + 5], packed[c * 8 + 6],
-                                 packed[c * 8 + 7]);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(out_stage + lane * 128 + ((j ^ (lane & 7)) << 4), packed[c * 32 + j * 4],
+                                     packed[c * 32 + j * 4 + 1], packed[c * 32 + j * 4 + 2], packed[c * 32 + j * 4 + 3]);
                     fence_proxy_async_shared();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&tmOut, buf, col_base + c * 16, row0, out_policy);
+                        tma_store_2d(&tmOut, out_stage, col_base + c * 64, row0, out_policy);
                         bulk_commit_group();
                     }
                 }
@@ -224,24 +242,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int ks = 0; ks < num_ks; ++ks) {
                 ok = __all_sync(~0u, mbar_wait(&full[stage], phase, p.err_flag, kErrTimeout, p.wait_ns));
                 if (!ok) break;
-                uint32_t a[16], b[32];
+                constexpr int kT = kSfTilesPerStage<kMx>;
+                uint32_t a[4 * kT], b[8 * kT];
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint4 v = ld_shared_v4(sfa_smem + stage * kSfaBytes + kk * 512);
-                    a[kk * 4 + 0] = v.x; a[kk * 4 + 1] = v.y; a[kk * 4 + 2] = v.z; a[kk * 4 + 3] = v.w;
+                for (int j = 0; j < kT; ++j) {
+                    const uint4 v = ld_shared_v4(sfa_smem + stage * kSfaBytes + j * 512);
+                    a[j * 4 + 0] = v.x; a[j * 4 + 1] = v.y; a[j * 4 + 2] = v.z; a[j * 4 + 3] = v.w;
                 }
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
+                for (int j = 0; j < kT; ++j)
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        const uint4 v = ld_shared_v4(sfb_smem + stage * kSfbBytes + h * 2048 + kk * 512);
-                        uint32_t *d = b + kk * 8 + h * 4;
+                        const uint4 v = ld_shared_v4(sfb_smem + stage * kSfbBytes + h * (kT * 512) + j * 512);
+                        uint32_t *d = b + j * 8 + h * 4;
                         d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
                     }
                 // (tiles past the valid K-steps, B rows or A rows hold stale
                 // bytes; what they meet in the MMA is never stored)
-                tmem_st_16cols(sf_tmem + stage * kSfColsPerStage, a);
-                tmem_st_32cols(sf_tmem + stage * kSfColsPerStage + 16, b);
+                if constexpr (kMx) {
+                    tmem_st_8cols(sf_tmem + stage * kSfColsPerStage, a);
+                    tmem_st_16cols(sf_tmem + stage * kSfColsPerStage + 4 * kT, b);
+                } else {
+                    tmem_st_16cols(sf_tmem + stage * kSfColsPerStage, a);
+                    tmem_st_32cols(sf_tmem + stage * kSfColsPerStage + 4 * kT, b);
+                }
                 tmem_st_wait();
                 tc_fence_before_sync();
                 __syncwarp();
@@ -272,28 +296,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Tile t = tile_coord(tile, p.num_m_blk, p.num_n_blk);
                 const int band_a = t.mb * 2 + (int)rank;
                 const bool a_here = band_a < a_bands;
-                const int halves = min(kTileN, p.n_out - t.nb * kTileN) > 128 ? 2 : 1;
                 for (int ks = 0; ks < num_ks; ++ks) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, p.err_flag, kErrTimeout, p.wait_ns)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t sf_bytes = (uint32_t)min(4, p.num_k64 - ks * 4) * 512;
+                    constexpr int kT = kSfTilesPerStage<kMx>;
+                    const uint32_t sf_bytes = (uint32_t)min(kT, p.sf_tiles - ks * kT) * 512;
                     if (act_side) {
                         mbar_arrive_expect_tx(&full[stage], kABytes + (a_here ? sf_bytes : 0));
                         tma_load_2d(smem + kOffA + stage * kABytes, &tmA, &full[stage], ks * kBKBytes, band_a * kRowsCta,
                                     pol);
                         if (a_here)
                             bulk_load(smem + kOffSfa + stage * kSfaBytes,
-                                      p.sfa + band_a * p.sfa_band_bytes + (int64_t)ks * 2048, sf_bytes, &full[stage], pol);
+                                      p.sfa + band_a * p.sfa_band_bytes + (int64_t)ks * kT * 512, sf_bytes, &full[stage], pol);
                     } else {
-                        mbar_arrive_expect_tx(&full[stage], kBBytes + sf_bytes * halves);
+                        // the stage's scale tiles of both B bands in one 2-D copy
+                        // (8-byte elements: box of kT tiles x 2 bands; past the
+                        // last band or K-step the TMA fills zeros)
+                        mbar_arrive_expect_tx(&full[stage], kBBytes + 2 * kT * 512);
                         tma_load_2d(smem + kOffB + stage * kBBytes, &tmB, &full[stage], ks * kBKBytes,
                                     t.nb * kTileN + (int)rank * kRowsCta, pol);
-                        for (int h = 0; h < halves; ++h)
-                            bulk_load(smem + kOffSfb + stage * kSfbBytes + h * 2048,
-                                      p.sfb + (t.nb * 2 + h) * p.sfb_band_bytes + (int64_t)ks * 2048, sf_bytes,
-                                      &full[stage], pol);
+                        tma_load_2d(smem + kOffSfb + stage * kSfbBytes, &tmSfb, &full[stage], ks * kT * 64, t.nb * 2,
+                                    pol);
                     }
                     issued_mask |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -345,9 +370,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t adesc = smem_desc_sw128(a_base + stage * kABytes);
                     const uint64_t bdesc = smem_desc_sw128(b_base + stage * kBBytes);
                     if (issuer) {
-                        for (int kk = 0; kk < kcount; ++kk)
-                            tc_mma_pair_nvf4(tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc,
-                                             sf_col + kk * 4, sf_col + 16 + kk * 8, (ks | kk) != 0);
+                        for (int kk = 0; kk < kcount; ++kk) {
+                            const uint64_t ad = adesc + (uint64_t)(kk * 2), bd = bdesc + (uint64_t)(kk * 2);
+                            if constexpr (kMx)      // two UE8M0 scales per row and K-step: half a scale word
+                                tc_mma_pair_mxf4(tmem, ad, bd, idesc_mxf4(kTileM, kTileN, (kk & 1) * 2),
+                                                 sf_col + (kk >> 1) * 4, sf_col + 8 + (kk >> 1) * 8, (ks | kk) != 0);
+                            else
+                                tc_mma_pair_nvf4(tmem, ad, bd, idesc, sf_col + kk * 4, sf_col + 16 + kk * 8,
+                                                 (ks | kk) != 0);
+                        }
                         tc_commit_pair_multicast(&empty[stage], kBothCtas);
                     }
                     if (++stage == kStages) { stage = 0; phase ^= 1; }
@@ -380,8 +411,11 @@ cudaError_t launch_gemm_pair(const GemmParams &p_in, const uint8_t *a, const uin
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_nvf4_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(gemm_nvf4_pair_kernel<false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gemm_nvf4_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kSmemBytes);
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t probe = {};
         cudaLaunchAttribute attr;
@@ -395,7 +429,7 @@ cudaError_t launch_gemm_pair(const GemmParams &p_in, const uint8_t *a, const uin
         probe.attrs = &attr;
         probe.numAttrs = 1;
         int clusters = 0;
-        e = cudaOccupancyMaxActiveClusters(&clusters, gemm_nvf4_pair_kernel, &probe);
+        e = cudaOccupancyMaxActiveClusters(&clusters, gemm_nvf4_pair_kernel<false>, &probe);
         if (e != cudaSuccess || clusters < 1) {
             cudaGetLastError();
             clusters = num_sms / 2;
@@ -409,14 +443,19 @@ cudaError_t launch_gemm_pair(const GemmParams &p_in, const uint8_t *a, const uin
     }
     GemmParams p = p_in;
     p.num_m_blk = (p.m + kTileM - 1) / kTileM;
-    CUtensorMap tmA, tmB, tmOut;
+    CUtensorMap tmA, tmB, tmSfb, tmOut;
     const uint64_t row_bytes = (uint64_t)p.kp / 2;
     if (!make_operand_map(&tmA, a, row_bytes, (uint64_t)p.m, kRowsCta) ||
         !make_operand_map(&tmB, w, row_bytes, (uint64_t)p.n_w, kRowsCta)) {
         *why = "cuTensorMapEncodeTiled failed for an FP4 operand";
         return cudaErrorInvalidValue;
     }
-    if (!make_output_map(&tmOut, p.out, (uint64_t)p.n_out, (uint64_t)p.m, (uint64_t)p.ldo)) {
+    const uint32_t sf_box = (uint32_t)(p.mx ? kSfTilesPerStage<true> : kSfTilesPerStage<false>) * 64;
+    if (!make_scale_bands_map(&tmSfb, p.sfb, (uint64_t)p.sfb_band_bytes, (uint64_t)(p.n_w + 127) / 128, sf_box)) {
+        *why = "cuTensorMapEncodeTiled failed for the weight scales";
+        return cudaErrorInvalidValue;
+    }
+    if (!make_output_map_sw128(&tmOut, p.out, (uint64_t)p.n_out, (uint64_t)p.m, (uint64_t)p.ldo)) {
         *why = "cuTensorMapEncodeTiled failed for the output";
         return cudaErrorInvalidValue;
     }
@@ -436,7 +475,8 @@ cudaError_t launch_gemm_pair(const GemmParams &p_in, const uint8_t *a, const uin
     cfg.stream = s;
     cfg.attrs = attrs;
     cfg.numAttrs = dependent ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, gemm_nvf4_pair_kernel, tmA, tmB, tmOut, p);
+    return p.mx ? cudaLaunchKernelEx(&cfg, gemm_nvf4_pair_kernel<true>, tmA, tmB, tmSfb, tmOut, p)
+                : cudaLaunchKernelEx(&cfg, gemm_nvf4_pair_kernel<false>, tmA, tmB, tmSfb, tmOut, p);
 }
 
 }  // namespace nvfp4
