@@ -604,7 +604,9 @@ def run_sweep(args, rank, dev, stream):
     import nvfp4_quantized_linear_gb300 as nv
     from nvfp4_quantized_linear_gb300 import synthetic as syn
     out = []
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    # a 256 MB read before each timed step evicts the previous step's lines
+    # (clean ones: a write-based flush would leave write-backs to compete)
+    flush = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
     for m in [1, 16, 128, 1024]:
         layers = []
         for p in layer_problems("llama", m, rank):
@@ -616,32 +618,53 @@ def run_sweep(args, rank, dev, stream):
             o = torch.empty((p.m, p.n), dtype=torch.bfloat16, device=dev)
             layers.append((p, L.x, gs_x, alpha, w_fp4, w_sf, ws, o))
 
-        def step():
+        def step(s):
             for p, x, gs_x, alpha, w_fp4, w_sf, ws, o in layers:
                 nv.nvfp4_linear(x, p.m, p.k, p.k, gs_x, None, 0, w_fp4, w_sf, p.n, p.n, alpha, None, o, p.n,
-                                ws, ws.numel(), stream)
+                                ws, ws.numel(), s)
 
         for _ in range(3):
-            step()
+            step(stream)
+        torch.cuda.synchronize()
+        # The step as a serving engine runs it: captured once in a CUDA graph
+        # and replayed (the CPU does not issue each launch).
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            step(side.cuda_stream)
+        torch.cuda.current_stream().wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step(torch.cuda.current_stream().cuda_stream)
         torch.cuda.synchronize()
         # The four layers' weights (~116 MB of FP4 + scales) would stay in the
         # 129 MB L2 across back-to-back steps; a real decoder streams them from
         # HBM, so L2 is flushed before every timed step.
         iters = 30
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
-        for e0, e1 in evs:
-            flush.zero_()
-            e0.record()
-            step()
-            e1.record()
-        torch.cuda.synchronize()
-        t = sum(e0.elapsed_time(e1) for e0, e1 in evs) / 1e3 / iters
+        timings = {}
+        for mode in ("graph", "eager"):
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+            for e0, e1 in evs:
+                flush.sum()
+                e0.record()
+                if mode == "graph":
+                    graph.replay()
+                else:
+                    step(stream)
+                e1.record()
+            torch.cuda.synchronize()
+            timings[mode] = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs) / 1e3
+        nv.nvfp4_device_error()
+        t = timings["graph"]
         flops = sum(p.flops for p, *_ in layers)
         wbytes = sum(w.numel() + s.numel() for _, _, _, _, w, s, _, _ in layers)
         abytes = sum(quant_bytes(p.m, p.k) + 2 * p.m * p.n for p, *_ in layers)
-        out.append({"workload": "llama3.1-8b", "m": m, "us_per_step": round(t * 1e6, 2), "tflops": round(flops / t / 1e12, 2),
-                    "algorithmic_gbs": round((wbytes + abytes) / t / 1e9, 1), "l2": "flushed before each step"})
-        del layers
+        out.append({"workload": "llama3.1-8b", "m": m, "us_per_step": round(t * 1e6, 2),
+                    "tflops": round(flops / t / 1e12, 2), "algorithmic_gbs": round((wbytes + abytes) / t / 1e9, 1),
+                    "us_per_step_eager": round(timings["eager"] * 1e6, 2),
+                    "launch": "CUDA graph replay of the 4-layer step (eager launches: us_per_step_eager)",
+                    "l2": "256 MB read before each step"})
+        del layers, graph
     return out
 
 
