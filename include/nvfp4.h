@@ -270,6 +270,38 @@ nvfp4_status nvfp4_gemm_ex(const uint8_t *a_fp4, const uint8_t *a_sf, int64_t m,
                            void *out_bf16, int64_t ldo, int kernel, uint64_t wait_limit_ns, int drill,
                            nvfp4_stream_t stream);
 
+/* Grouped NVFP4 GEMM for mixture-of-experts layers: one launch over the
+ * token groups of all experts, each group multiplied by its own expert's
+ * weight (the grouped NVFP4 MoE GEMM the transform page's related-work
+ * section points to; the b12x page's packed-weight reuse keeps the stacked
+ * weights in place).  The pages give no formula beyond nvfp4_gemm's, applied
+ * per group:
+ *   out[r, j] = bf16( alpha[g] * sum_k deq(A)[r,k] * deq(W)[g*n + j, k] + bias[g*n + j] )
+ * for the rows r of group g and j < n.
+ *   a_fp4, a_sf        in   activations of every group in one [rows, k] operand
+ *                           (nvfp4_quant_act of the stacked rows, one global scale)
+ *   group_offsets_dev  in   device int32 [num_groups + 1], ascending multiples
+ *                           of 128: group g owns rows [offsets[g], offsets[g+1]),
+ *                           the groups' real rows first and any padding rows
+ *                           after them; 128-row bands at or past
+ *                           offsets[num_groups] are not computed.  Being on the
+ *                           device, the offsets can come from a routing kernel
+ *                           of the same stream (no host synchronisation).
+ *   w_fp4, w_sf        in   the experts' weights stacked as one [num_groups*n, k]
+ *                           operand (nvfp4_prepare_weight per expert into the
+ *                           slices w_fp4 + g*n*Kp/2 and w_sf + g*n*Cp, or once
+ *                           over all of them); n a multiple of 128
+ *   alpha_dev          in   device fp32 [num_groups]: 1/(gs_x * gs_w[g])
+ *   bias_bf16          in   NULL or [num_groups * n] bf16
+ *   out_bf16           out  [rows, ldo] bf16; every row of every computed band is
+ *                           written (padding rows get unspecified values)
+ * One 128 x 256 output tile per CTA step on the one-CTA kernel; no split-K. */
+nvfp4_status nvfp4_grouped_gemm(const uint8_t *a_fp4, const uint8_t *a_sf, int64_t rows,
+                                const int32_t *group_offsets_dev, int num_groups,
+                                const uint8_t *w_fp4, const uint8_t *w_sf, int64_t n, int64_t k,
+                                const float *alpha_dev, const void *bias_bf16,
+                                void *out_bf16, int64_t ldo, nvfp4_stream_t stream);
+
 /* The whole linear layer (torch-backend page apply_weights; b12x page
  * _apply_b12x_nvfp4_linear): nvfp4_quant_act of x into `workspace`, then
  * the GEMM of nvfp4_gemm, all on `stream`.  workspace (device) is scratch owned

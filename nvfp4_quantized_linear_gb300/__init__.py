@@ -24,7 +24,7 @@ __all__ = [
     "nvfp4_packed_bytes", "nvfp4_scale_bytes", "nvfp4_linear_workspace_bytes",
     "nvfp4_prepare_weight", "nvfp4_quant_act", "nvfp4_quant_act_export_y", "nvfp4_act_global_scale", "nvfp4_mxfp4_scale_bytes", "nvfp4_mxfp4_quant_act",
     "nvfp4_mxfp4_gemm", "nvfp4_mxfp4_linear_workspace_bytes", "nvfp4_mxfp4_linear", "mxfp4_linear",
-    "nvfp4_gemm", "nvfp4_gemm_ex", "nvfp4_linear", "nvfp4_linear_noalloc",
+    "nvfp4_gemm", "nvfp4_gemm_ex", "nvfp4_grouped_gemm", "nvfp4_linear", "nvfp4_linear_noalloc",
     "padded_k", "scale_shape", "quant_act", "quant_act_mx", "prepare_weight", "linear", "act_global_scale",
 ]
 
@@ -58,6 +58,7 @@ EXPORTS = [
     ("nvfp4_mxfp4_linear_workspace_bytes", _SZ, [_I64, _I64, _I64]),
     ("nvfp4_mxfp4_linear", _I32, [_P, _I64, _I64, _I64, _P, _P, _I64, _I64, _P, _P, _I64, _P, _SZ, _P]),
     ("nvfp4_gemm", _I32, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _P, _P, _I64, _P]),
+    ("nvfp4_grouped_gemm", _I32, [_P, _P, _I64, _P, _I32, _P, _P, _I64, _I64, _P, _P, _P, _I64, _P]),
     ("nvfp4_gemm_ex", _I32, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _P, _P, _I64, _I32, ctypes.c_uint64, _I32,
                              _P]),
     ("nvfp4_linear", _I32, [_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _I64, _I64, _P, _P, _P, _I64,
@@ -223,6 +224,13 @@ def nvfp4_gemm(a_fp4, a_sf, m: int, w_fp4, w_sf, n_w: int, n_out: int, k: int, a
                stream=None) -> None:
     _check(load_library().nvfp4_gemm(_ptr(a_fp4), _ptr(a_sf), m, _ptr(w_fp4), _ptr(w_sf), n_w, n_out, k,
                                      _ptr(alpha), _ptr(bias), _ptr(out), ldo, _stream(stream)))
+
+
+def nvfp4_grouped_gemm(a_fp4, a_sf, rows: int, group_offsets, num_groups: int, w_fp4, w_sf, n: int, k: int, alpha,
+                       bias, out, ldo: int, stream=None) -> None:
+    _check(load_library().nvfp4_grouped_gemm(_ptr(a_fp4), _ptr(a_sf), rows, _ptr(group_offsets), num_groups,
+                                             _ptr(w_fp4), _ptr(w_sf), n, k, _ptr(alpha), _ptr(bias), _ptr(out), ldo,
+                                             _stream(stream)))
 
 
 def nvfp4_gemm_ex(a_fp4, a_sf, m: int, w_fp4, w_sf, n_w: int, n_out: int, k: int, alpha, bias, out, ldo: int,

@@ -246,6 +246,9 @@ nvfp4::GemmParams gemm_params(const uint8_t *a_sf, int64_t m, const uint8_t *w_s
     g.stages_per_split = (g.num_k64 + 3) / 4;
     g.partials = nullptr;
     g.part_ld = 0;
+    g.group_offsets = nullptr;
+    g.num_groups = 0;
+    g.group_n = 0;
     g.wait_ns = nvfp4::kDefaultWaitNs;
     g.drill = 0;
     return g;
@@ -677,6 +680,48 @@ nvfp4_status nvfp4_mxfp4_linear(const void *x_bf16, int64_t m, int64_t k, int64_
     float *partials = workspace_bytes > need ? reinterpret_cast<float *>(ws + need) : nullptr;
     return run_gemm(a_fp4, a_sf, m, w_fp4, w_sf, n_w, n_out, k, nullptr, bias_bf16, out_bf16, ldo, num_sms, s,
                     partials, workspace_bytes > need ? workspace_bytes - need : 0, true, kGemmAuto, 0, 0, true);
+}
+
+nvfp4_status nvfp4_grouped_gemm(const uint8_t *a_fp4, const uint8_t *a_sf, int64_t rows,
+                                const int32_t *group_offsets_dev, int num_groups, const uint8_t *w_fp4,
+                                const uint8_t *w_sf, int64_t n, int64_t k, const float *alpha_dev,
+                                const void *bias_bf16, void *out_bf16, int64_t ldo, nvfp4_stream_t stream)
+{
+    if (num_groups < 1 || num_groups > (1 << 16))
+        return fail(NVFP4_ERR_INVALID_ARG, "num_groups must be in [1, 65536] (got %d)", num_groups);
+    if (n < 128 || n % 128 != 0 || n * (int64_t)num_groups > kMaxDim)
+        return fail(NVFP4_ERR_INVALID_ARG, "n must be a positive multiple of 128 with num_groups * n < 2^31 (got %lld)",
+                    (long long)n);
+    nvfp4_status st = check_gemm_args(rows > 0 ? a_fp4 : nullptr, rows > 0 ? a_sf : nullptr, rows, w_fp4, w_sf,
+                                      n * num_groups, n, k, alpha_dev, bias_bf16, out_bf16, ldo);
+    if (st != NVFP4_OK) return st;
+    if (rows == 0) return ok();
+    if (!a_fp4 || !a_sf || !alpha_dev || !group_offsets_dev)
+        return fail(NVFP4_ERR_INVALID_ARG, "null pointer argument");
+    if ((reinterpret_cast<uintptr_t>(group_offsets_dev) & 3) || (reinterpret_cast<uintptr_t>(alpha_dev) & 3))
+        return fail(NVFP4_ERR_ALIGNMENT, "group offsets and alphas must be 4-byte aligned");
+    const int64_t wrows = n * num_groups;
+    Range outs[1] = {range2d(out_bf16, rows, n, ldo, "out")};
+    Range ins[7] = {range(a_fp4, nvfp4_packed_bytes(rows, k), "a_fp4"), range(a_sf, nvfp4_scale_bytes(rows, k), "a_sf"),
+                    range(w_fp4, nvfp4_packed_bytes(wrows, k), "w_fp4"),
+                    range(w_sf, nvfp4_scale_bytes(wrows, k), "w_sf"),
+                    range(alpha_dev, (size_t)num_groups * 4, "alpha"),
+                    range(bias_bf16, bias_bf16 ? (size_t)wrows * 2 : 0, "bias"),
+                    range(group_offsets_dev, (size_t)(num_groups + 1) * 4, "group_offsets")};
+    if ((st = check_aliases(outs, 1, ins, 7)) != NVFP4_OK) return st;
+    int num_sms = 0;
+    if ((st = current_device(&num_sms)) != NVFP4_OK) return st;
+    unsigned int *err = nullptr;
+    cudaError_t e = nvfp4::device_error_word(&err);
+    if (e != cudaSuccess) return launch_status(e, "grouped GEMM (error word)");
+    nvfp4::GemmParams g = gemm_params(a_sf, rows, w_sf, wrows, n, k, alpha_dev, bias_bf16, out_bf16, ldo, err);
+    g.group_offsets = group_offsets_dev;
+    g.num_groups = num_groups;
+    g.group_n = (int32_t)n;
+    const char *why = nullptr;
+    e = nvfp4::launch_gemm(g, a_fp4, w_fp4, num_sms, reinterpret_cast<cudaStream_t>(stream), &why, false);
+    if (why) return fail(NVFP4_ERR_CUDA, "%s", why);
+    return launch_status(e, "grouped GEMM kernel");
 }
 
 }  // extern "C"

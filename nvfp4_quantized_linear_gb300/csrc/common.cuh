@@ -65,6 +65,16 @@ struct GemmParams {
     int32_t stages_per_split;
     float *partials;
     int64_t part_ld;
+    // Grouped GEMM (one-CTA kernel only): group_offsets [num_groups + 1] are
+    // ascending row offsets, multiples of 128; the 128-row band of A at row r
+    // belongs to the group g with offsets[g] <= r < offsets[g + 1] and is
+    // multiplied by weight rows [g * group_n, (g + 1) * group_n) (stacked
+    // weights), scaled by alpha[g], biased by bias[g * group_n + column].
+    // Bands at or past offsets[num_groups] are skipped.  group_offsets ==
+    // nullptr: a plain GEMM (group 0, group_n = 0).
+    const int32_t *group_offsets;
+    int32_t num_groups;
+    int32_t group_n;
     uint64_t wait_ns;                // bound of every pipeline barrier wait (ns of %globaltimer)
     int32_t drill;                   // 1: timeout drill, the producers issue no copies (test hook)
 };

@@ -85,11 +85,27 @@ static_assert(128 * (kRegsCtl + kRegsSf + 2 * kRegsEpi) <= kThreads * 128, "regi
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffOut % 128 == 0, "TMA store sources are 128-byte aligned");
 
-// Work item of a persistent CTA: output tile and K-stage range [ks0, ks1).
+// Work item of a persistent CTA: output tile, K-stage range [ks0, ks1) and,
+// for a grouped GEMM, the group of the tile's row band (-1: no group, skip).
 struct Work {
     Tile t;
-    int split, ks0, ks1;
+    int split, ks0, ks1, g;
 };
+
+// Group of the 128-row band mb: the last g with offsets[g] <= 128 mb, or -1
+// for a band outside [offsets[0], offsets[num_groups]).
+__device__ __forceinline__ int group_of_band(const GemmParams &p, int mb)
+{
+    const int row = mb * 128;
+    if (row < __ldg(p.group_offsets) || row >= __ldg(p.group_offsets + p.num_groups)) return -1;
+    int lo = 0, hi = p.num_groups - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(p.group_offsets + mid) <= row) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
 
 __device__ __forceinline__ Work work_of(int item, const GemmParams &p, int num_ks)
 {
@@ -99,6 +115,7 @@ __device__ __forceinline__ Work work_of(int item, const GemmParams &p, int num_k
     w.t = tile_coord(item - w.split * per_split, p.num_m_blk, p.num_n_blk);
     w.ks0 = w.split * p.stages_per_split;
     w.ks1 = min(num_ks, w.ks0 + p.stages_per_split);
+    w.g = p.group_offsets != nullptr ? group_of_band(p, w.t.mb) : 0;
     return w;
 }
 
@@ -171,12 +188,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t acc = tmem + ((uint32_t)(q * 32) << 16) + hcol;
         const uint32_t out_stage = smem_u32(smem + kOffOut) + (warp - kEpiWarp0) * kOutChunkBytes;
         const bool use_bias = p.splits == 1 && p.bias != nullptr;
-        const float alpha = p.alpha != nullptr ? __ldg(p.alpha) : 1.0f;
         const uint64_t out_policy = l2_policy_evict_first();   // the output is written once
         uint32_t acc_phase = 0;
         int it = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
             const Work wk = work_of(tile, p, num_ks);
+            if (wk.g < 0) continue;                             // every role skips the same tiles
+            const float alpha = p.alpha != nullptr ? __ldg(p.alpha + wk.g) : 1.0f;
             const Tile t = wk.t;
             const int n_cols = min(kEpiCols, p.n_out - t.nb * kBN - hcol);   // may be <= 0
             const int col_base = t.nb * kBN + hcol;
@@ -289,6 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
             const Work wk = work_of(tile, p, num_ks);
+            if (wk.g < 0) continue;
             for (int ks = wk.ks0; ks < wk.ks1; ++ks) {
                 ok = __all_sync(~0u, mbar_wait(&full[stage], phase, p.err_flag, kErrTimeout, p.wait_ns));
                 if (!ok) break;
@@ -346,7 +365,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
                 const Work wk = work_of(tile, p, num_ks);
+                if (wk.g < 0) continue;
                 const Tile t = wk.t;
+                const int b_row0 = wk.g * p.group_n + t.nb * kBN;          // weight rows of this tile
+                const int b_band0 = b_row0 / 128;
                 const int halves = min(kBN, p.n_out - t.nb * kBN) > 128 ? 2 : 1;
                 for (int ks = wk.ks0; ks < wk.ks1; ++ks) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, p.err_flag, kErrTimeout, p.wait_ns)) { ok = false; break; }
@@ -359,10 +381,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   p.sfa + t.mb * p.sfa_band_bytes + (int64_t)ks * kT * 512, sf_bytes, &full[stage], pol);
                     } else {
                         mbar_arrive_expect_tx(&full[stage], kBBytes + sf_bytes * halves);
-                        tma_load_2d(smem + kOffB + stage * kBBytes, &tmB, &full[stage], ks * kBKBytes, t.nb * kBN, pol);
+                        tma_load_2d(smem + kOffB + stage * kBBytes, &tmB, &full[stage], ks * kBKBytes, b_row0, pol);
                         for (int h = 0; h < halves; ++h)    // halves == 2 implies band t.nb*2+1 exists
                             bulk_load(smem + kOffSfb + stage * kSfbBytes + h * 2048,
-                                      p.sfb + (t.nb * 2 + h) * p.sfb_band_bytes + (int64_t)ks * kT * 512, sf_bytes,
+                                      p.sfb + (int64_t)(b_band0 + h) * p.sfb_band_bytes + (int64_t)ks * kT * 512, sf_bytes,
                                       &full[stage], pol);
                     }
                     issued_mask |= 1u << stage;
@@ -382,14 +404,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint16_t *s_bias_all = reinterpret_cast<uint16_t *>(smem + kOffBias);
             int it = 0;
             for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
-                const Tile t = work_of(tile, p, num_ks).t;
+                const Work wk = work_of(tile, p, num_ks);
+                if (wk.g < 0) continue;
+                const Tile t = wk.t;
                 const int n_rows = min(kBN, p.n_out - t.nb * kBN);
                 const int b = it & 1;
                 if (!__all_sync(~0u, mbar_wait(&bias_empty[b], ((it >> 1) & 1) ^ 1, p.err_flag, kErrTimeout,
                                                p.wait_ns)))
                     break;
                 for (int j = lane; j < kBN; j += 32)
-                    s_bias_all[b * kBN + j] = (j < n_rows) ? p.bias[t.nb * kBN + j] : (uint16_t)0;
+                    s_bias_all[b * kBN + j] = (j < n_rows) ? p.bias[wk.g * p.group_n + t.nb * kBN + j] : (uint16_t)0;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bias_full[b]);
             }
@@ -406,6 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
                 const Work wk = work_of(tile, p, num_ks);
+                if (wk.g < 0) continue;
                 const int n_rows = min(kBN, p.n_out - wk.t.nb * kBN);
                 const uint32_t n_mma = n_rows > 128 ? 256 : 128;
                 const uint32_t idesc = idesc_nvf4(128, n_mma);

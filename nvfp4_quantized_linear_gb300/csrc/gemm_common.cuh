@@ -25,9 +25,11 @@ constexpr int kSfTilesPerStage = kMx ? 2 : 4;
 // bands, so each weight tile is streamed from DRAM about once and shared by
 // the row bands through L2, while the group's activation rows (at most 64
 // bands) stay resident in L2 across columns.
+constexpr int kTileGroupBands = 64;   // row bands per group of the tile walk
+
 __device__ __forceinline__ Tile tile_coord(int tile, int num_m, int num_n)
 {
-    const int G = num_m < 64 ? num_m : 64;
+    const int G = num_m < kTileGroupBands ? num_m : kTileGroupBands;
     const int per_group = G * num_n;
     const int group = tile / per_group;
     const int first_m = group * G;
