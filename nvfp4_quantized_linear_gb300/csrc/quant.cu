@@ -372,6 +372,11 @@ __global__ void __launch_bounds__(kXfThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int bs = p.bs;
+    const int n_ct = (p.nbp * 16 + kXfCols - 1) / kXfCols;   // covers every scale column
+    const int num_tiles = (p.mp / kXfRows) * n_ct;
+    // x is read once; the amax pass leaves it in L2 for the quantizer that follows
+    const uint64_t x_pol = kAmaxOnly ? l2_policy_evict_normal() : l2_policy_evict_first();
+    int pre_issued = 0;                           // (thread 0, the producer) stages issued before the role split
     if (threadIdx.x == 0) {
         griddep_launch_dependents();              // as in quant_kernel
         for (int s = 0; s < kXfStages; ++s) {
@@ -385,6 +390,15 @@ __global__ void __launch_bounds__(kXfThreads, 1)
         mbar_init(mma_done, 1);
         fence_mbarrier_init();
         prefetch_tensormap(&tmX);
+        // The first stages' x tiles are requested now, so that they load while
+        // the block stages T and allocates its TMEM (their stages are free).
+        for (int tile = blockIdx.x; tile < num_tiles && pre_issued < kXfStages; tile += gridDim.x, ++pre_issued) {
+            const int rb = tile / n_ct, ct = tile - rb * n_ct;
+            uint8_t *dst = smem + pre_issued * kXfStageBytes;
+            mbar_arrive_expect_tx(&full[pre_issued], kXfStageBytes);
+            tma_load_2d(dst, &tmX, &full[pre_issued], ct * kXfCols, rb * kXfRows, x_pol);
+            tma_load_2d(dst + kXfBoxBytes, &tmX, &full[pre_issued], ct * kXfCols + 64, rb * kXfRows, x_pol);
+        }
     }
     // T^T into shared memory: element T[i][n] -> row n, K index i, written
     // where the 128-byte swizzle puts it (16-byte chunk index XOR row % 8).
@@ -430,9 +444,6 @@ __global__ void __launch_bounds__(kXfThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-
-    const int n_ct = (p.nbp * 16 + kXfCols - 1) / kXfCols;   // covers every scale column
-    const int num_tiles = (p.mp / kXfRows) * n_ct;
 
     if (warp >= kXfEpiWarp0) {
         // ---------------------------------------------------------- epilogue --
@@ -521,10 +532,8 @@ __global__ void __launch_bounds__(kXfThreads, 1)
     } else if (warp == 0) {
         if (lane == 0) {
             // --------------------------------------------------------- producer --
-            // x is read once; the amax pass leaves it in L2 for the quantizer that follows
-            const uint64_t pol = kAmaxOnly ? l2_policy_evict_normal() : l2_policy_evict_first();
-            int it = 0;
-            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+            int it = pre_issued;
+            for (int tile = blockIdx.x + pre_issued * (int)gridDim.x; tile < num_tiles; tile += gridDim.x, ++it) {
                 const int stage = it % kXfStages;
                 if (!mbar_wait(&empty[stage], ((uint32_t)(it / kXfStages) & 1u) ^ 1u, p.err_flag, kErrTimeout,
                                kXfWaitNs))
@@ -532,8 +541,8 @@ __global__ void __launch_bounds__(kXfThreads, 1)
                 const int rb = tile / n_ct, ct = tile - rb * n_ct;
                 uint8_t *dst = smem + stage * kXfStageBytes;
                 mbar_arrive_expect_tx(&full[stage], kXfStageBytes);
-                tma_load_2d(dst, &tmX, &full[stage], ct * kXfCols, rb * kXfRows, pol);
-                tma_load_2d(dst + kXfBoxBytes, &tmX, &full[stage], ct * kXfCols + 64, rb * kXfRows, pol);
+                tma_load_2d(dst, &tmX, &full[stage], ct * kXfCols, rb * kXfRows, x_pol);
+                tma_load_2d(dst + kXfBoxBytes, &tmX, &full[stage], ct * kXfCols + 64, rb * kXfRows, x_pol);
             }
             // Every copy issued has landed before the CTA may exit (the last
             // issue of each stage is its newest phase).
