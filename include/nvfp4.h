@@ -312,7 +312,12 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t *a_fp4, const uint8_t *a_sf, int64
  * tiles to fill the GPU splits K across CTAs: each writes fp32 partial sums to
  * the workspace and a second kernel adds them in split order, then applies
  * alpha and bias.  The result is deterministic, but its fp32 rounding order
- * differs from the unsplit GEMM's (both are within the GEMM's accuracy). */
+ * differs from the unsplit GEMM's (both are within the GEMM's accuracy).
+ * For m <= 8 without a transform (decode batch sizes) the quantizer runs
+ * inside the GEMM: its activation warp quantizes each K stage of x into the
+ * MMA's shared-memory tile itself (the workspace's activation area is then
+ * not written).  Codes, scales and output are those of nvfp4_quant_act
+ * followed by nvfp4_gemm, bit for bit. */
 nvfp4_status nvfp4_linear(const void *x_bf16, int64_t m, int64_t k, int64_t ldx,
                           const float *gs_dev, const void *transform_bf16, int bs,
                           const uint8_t *w_fp4, const uint8_t *w_sf, int64_t n_w, int64_t n_out,

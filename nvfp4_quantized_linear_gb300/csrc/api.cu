@@ -316,7 +316,7 @@ nvfp4_status run_gemm(const uint8_t *a, const uint8_t *a_sf, int64_t m, const ui
                       int64_t n_w, int64_t n_out, int64_t k, const float *alpha, const void *bias, void *out,
                       int64_t ldo, int num_sms, cudaStream_t s, float *partials = nullptr, size_t partial_bytes = 0,
                       bool after_quant = false, int kernel = kGemmAuto, uint64_t wait_ns = 0, int drill = 0,
-                      bool mx = false)
+                      bool mx = false, const nvfp4::QuantParams *fuse_quant = nullptr)
 {
     unsigned int *err = nullptr;
     cudaError_t e = nvfp4::device_error_word(&err);
@@ -336,10 +336,15 @@ nvfp4_status run_gemm(const uint8_t *a, const uint8_t *a_sf, int64_t m, const ui
     }
     const char *why = nullptr;
     const bool pair = kernel == kGemmPair || (kernel == kGemmAuto && m > 128);
-    e = pair ? nvfp4::launch_gemm_pair(g, a, w, num_sms, s, &why, after_quant)
-             : nvfp4::launch_gemm(g, a, w, num_sms, s, &why, after_quant);
+    if (fuse_quant != nullptr) {                     // the fused small-m linear: quantizer inside the GEMM
+        g.quant = *fuse_quant;
+        e = nvfp4::launch_linear_fused(g, w, num_sms, s, &why);
+    } else {
+        e = pair ? nvfp4::launch_gemm_pair(g, a, w, num_sms, s, &why, after_quant)
+                 : nvfp4::launch_gemm(g, a, w, num_sms, s, &why, after_quant);
+    }
     if (why) return fail(NVFP4_ERR_CUDA, "%s", why);
-    nvfp4_status st = launch_status(e, "GEMM kernel");
+    nvfp4_status st = launch_status(e, fuse_quant ? "fused linear kernel" : "GEMM kernel");
     if (st != NVFP4_OK || g.splits == 1) return st;
     return launch_status(nvfp4::launch_splitk_reduce(g, num_sms, s), "split-K reduce kernel");
 }
@@ -607,12 +612,17 @@ nvfp4_status nvfp4_linear(const void *x_bf16, int64_t m, int64_t k, int64_t ldx,
     int num_sms = 0;
     if ((st = current_device(&num_sms)) != NVFP4_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    st = run_quant(quant_params(x_bf16, m, k, ldx, gs_dev, transform_bf16, bs, a_fp4, a_sf), num_sms, s);
-    if (st != NVFP4_OK) return st;
+    const nvfp4::QuantParams qp = quant_params(x_bf16, m, k, ldx, gs_dev, transform_bf16, bs, a_fp4, a_sf);
     // the rest of the workspace (if any) takes split-K partial sums
     float *partials = workspace_bytes > need ? reinterpret_cast<float *>(ws + need) : nullptr;
+    const size_t partial_bytes = workspace_bytes > need ? workspace_bytes - need : 0;
+    if (m <= 8 && transform_bf16 == nullptr)        // decode sizes: the GEMM quantizes its own activation
+        return run_gemm(a_fp4, a_sf, m, w_fp4, w_sf, n_w, n_out, k, alpha_dev, bias_bf16, out_bf16, ldo, num_sms,
+                        s, partials, partial_bytes, false, kGemmAuto, 0, 0, false, &qp);
+    st = run_quant(qp, num_sms, s);
+    if (st != NVFP4_OK) return st;
     return run_gemm(a_fp4, a_sf, m, w_fp4, w_sf, n_w, n_out, k, alpha_dev, bias_bf16, out_bf16, ldo, num_sms, s,
-                    partials, workspace_bytes > need ? workspace_bytes - need : 0, true);
+                    partials, partial_bytes, true);
 }
 
 size_t nvfp4_mxfp4_linear_workspace_bytes(int64_t m, int64_t k, int64_t n_w)

@@ -77,6 +77,9 @@ struct GemmParams {
     int32_t group_n;
     uint64_t wait_ns;                // bound of every pipeline barrier wait (ns of %globaltimer)
     int32_t drill;                   // 1: timeout drill, the producers issue no copies (test hook)
+    // Fused small-m linear (one-CTA kernel): the activation the kernel
+    // quantizes itself, stage by stage, into shared memory.
+    QuantParams quant;
 };
 
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;   // two seconds
@@ -89,6 +92,13 @@ cudaError_t launch_quant_transform(const QuantParams &p, int num_sms, cudaStream
 // the GEMM's weight-side loads then start before that kernel has finished.
 cudaError_t launch_gemm(const GemmParams &p, const uint8_t *a, const uint8_t *w, int num_sms, cudaStream_t s,
                         const char **why, bool dependent = false);
+// The fused small-m linear (m <= 8, NVFP4, no transform): p.quant describes
+// the bf16 activation; the GEMM's activation warp quantizes each stage of it
+// into shared memory itself, so no quantizer runs before it.  Launched as a
+// programmatic dependent of the kernel before it, whose completion both of its
+// producers wait for.  With splits > 1 the caller launches the split-K reduce.
+cudaError_t launch_linear_fused(const GemmParams &p, const uint8_t *w, int num_sms, cudaStream_t s,
+                                const char **why);
 // Sum of the split-K partials, then alpha, bias and bf16 rounding into out;
 // launched as a programmatic dependent of the split GEMM just before it.
 cudaError_t launch_splitk_reduce(const GemmParams &p, int num_sms, cudaStream_t s);

@@ -38,6 +38,7 @@
 #include "common.cuh"
 #include "gemm_common.cuh"
 #include "ptx.cuh"
+#include "quant_core.cuh"
 
 namespace nvfp4 {
 
@@ -68,7 +69,10 @@ constexpr uint32_t kOffBias = kOffSfb + kStages * kSfbBytes;   // two tiles of b
 constexpr uint32_t kOutChunkBytes = 32 * 16 * 2;              // output staging: 32 rows x 16 columns bf16
 constexpr uint32_t kOffOut = kOffBias + 2 * kBN * 2;          // per epilogue warp: one staging chunk
 constexpr uint32_t kOffBar = kOffOut + 8 * kOutChunkBytes;
-constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;   // barriers + alignment slack
+constexpr uint32_t kOffInvTab = kOffBar + 256;          // fused linear: gs / e4m3(code) for the 128 codes
+constexpr uint32_t kSmemBytes = kOffInvTab + 512 + 1024;   // + alignment slack
+constexpr int kFusedMaxRows = 8;                           // the fused linear's largest m
+constexpr int kXSliceRows = 16;                             // rows of the fused linear's activation copies
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemSf = 256;
 constexpr uint32_t kSfColsPerStage = 48;
@@ -119,13 +123,127 @@ __device__ __forceinline__ Work work_of(int item, const GemmParams &p, int num_k
     return w;
 }
 
+// Sum of the split-K partials, then alpha, bias and bf16 rounding, for the
+// items (row, four columns) i = first, first + stride, ...: out[r, c] =
+// bf16(alpha * sum_s partials[s][r][c] + bias[c]), the splits added in index
+// order (deterministic), every split's load issued before the sum.
+__device__ __forceinline__ void reduce_partials(const GemmParams &p, int64_t first, int64_t stride)
+{
+    const float alpha = p.alpha != nullptr ? __ldg(p.alpha) : 1.0f;
+    const int groups = (p.n_out + 3) / 4;
+    const int64_t total = (int64_t)p.m * groups;
+    const int64_t split_stride = (int64_t)p.m * p.part_ld;
+    for (int64_t i = first; i < total; i += stride) {
+        const int64_t r = i / groups;
+        const int c = (int)(i - r * groups) * 4;
+        const float *src = p.partials + r * p.part_ld + c;
+        float4 v[kMaxSplits];
+#pragma unroll
+        for (int sp = 0; sp < kMaxSplits; ++sp)
+            if (sp < p.splits) v[sp] = __ldcs(reinterpret_cast<const float4 *>(src + sp * split_stride));
+        float4 acc = v[0];
+#pragma unroll
+        for (int sp = 1; sp < kMaxSplits; ++sp)
+            if (sp < p.splits) { acc.x += v[sp].x; acc.y += v[sp].y; acc.z += v[sp].z; acc.w += v[sp].w; }
+        const float a[4] = {acc.x, acc.y, acc.z, acc.w};
+        uint16_t *o = p.out + r * p.ldo + c;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (c + e < p.n_out) {
+                const float b = p.bias ? __uint_as_float((uint32_t)p.bias[c + e] << 16) : 0.0f;
+                o[e] = (uint16_t)bf16_bits_rn(__fmaf_rn(a[e], alpha, b));
+            }
+    }
+}
+
+// The activation side of the fused small-m linear (the whole of warp 0): for
+// every stage of this CTA's work items, fetch the stage's 256 columns of the
+// m <= kFusedMaxRows activation rows (bf16, one 2-D TMA of 16 rows x 256
+// columns, zeros past m and k) into bytes [2 KB, 10 KB) of the stage's own A
+// tile -- the rows 16..127 of that tile, which the MMA reads but whose scales
+// are zero -- then quantize them exactly as quant_kernel does (one 16-element
+// block per lane and round) into the tile's first 16 rows (128-byte rows with
+// the TMA's 128-byte swizzle, the layout of the MMA's descriptor) and the
+// block scales into the stage's four scale tiles, zeroed first so that rows
+// >= m contribute nothing (their A bytes are finite FP4 codes whatever they
+// hold).  Then the async-proxy fence and the stage's second `full` arrival.
+// The slice's copy is requested when the stage frees, together with the
+// stage's weights, so it adds no latency of its own.
+constexpr uint32_t kXSliceOff = 16 * 128;                    // rows 16.. of an A tile
+constexpr uint32_t kXSliceBytes = kXSliceRows * 256 * 2;     // 16 rows x 256 bf16
+static_assert(kXSliceOff + kXSliceBytes <= kABytes, "the activation slice fits in the A tile's spare rows");
+
+template <bool kFused>
+__device__ __forceinline__ void fused_act_producer(const GemmParams &p, const CUtensorMap *tmX, uint8_t *smem,
+                                                   uint64_t *full, uint64_t *empty, uint64_t *x_full, int num_ks,
+                                                   int lane)
+{
+    griddep_wait();                                  // x and gs may be the preceding kernel's output
+    const QuantParams &q = p.quant;
+    const float gs = __ldg(q.gs);
+    const float *inv_tab = reinterpret_cast<const float *>(smem + kOffInvTab);
+    const uint64_t pol = l2_policy_evict_last();     // every column tile's CTAs read the same slices
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int tile = blockIdx.x; tile < p.num_m_blk * p.num_n_blk * p.splits; tile += gridDim.x) {
+        const Work wk = work_of(tile, p, num_ks);
+        for (int ks = wk.ks0; ks < wk.ks1; ++ks) {
+            if (!__all_sync(~0u, mbar_wait(&empty[stage], phase ^ 1, p.err_flag, kErrTimeout, p.wait_ns))) return;
+            uint8_t *a_tile = smem + kOffA + stage * kABytes;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&x_full[stage], kXSliceBytes);
+                tma_load_2d(a_tile + kXSliceOff, tmX, &x_full[stage], ks * 256, 0, pol);
+            }
+            const uint32_t a_dst = smem_u32(a_tile);
+            const uint32_t x_src = a_dst + kXSliceOff;
+            const uint32_t sf_dst = smem_u32(smem + kOffSfa + stage * kSfaBytes);
+#pragma unroll
+            for (int i = 0; i < (int)kSfaBytes / 16 / 32; ++i) st_shared_v4(sf_dst + (lane + 32 * i) * 16, 0, 0, 0, 0);
+            if (!__all_sync(~0u, mbar_wait(&x_full[stage], phase, p.err_flag, kErrTimeout, p.wait_ns))) return;
+            for (int b = lane; b < q.m * 16; b += 32) {
+                const int r = b >> 4, j = b & 15;
+                quant_core::Raw16 raw;
+                raw.a = ld_shared_v4(x_src + (uint32_t)r * 512 + (uint32_t)j * 32);
+                raw.b = ld_shared_v4(x_src + (uint32_t)r * 512 + (uint32_t)j * 32 + 16);
+                float v0[8], v1[8];
+                quant_core::unpack8(raw.a, v0);
+                quant_core::unpack8(raw.b, v1);
+                float amax = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(v0[i]), fabsf(v1[i])));
+                float inv;
+                const uint32_t sf = quant_core::block_scale_tab(amax, gs, inv_tab, inv);
+                const uint32_t lo = quant_core::quant8(v0, inv), hi = quant_core::quant8(v1, inv);
+                // packed bytes [8j, 8j + 8) of row r: 16-byte piece j / 2 of the
+                // row, at piece (j / 2) ^ (r % 8) after the swizzle
+                const uint32_t a_off = (uint32_t)(r >> 3) * 1024 + (uint32_t)(r & 7) * 128 +
+                                       ((uint32_t)((j >> 1) ^ (r & 7)) << 4) + (uint32_t)(j & 1) * 8;
+                asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(a_dst + a_off), "r"(lo), "r"(hi) : "memory");
+                // scale column j of the stage: tile j / 4, the tiled layout inside it
+                const uint32_t sf_off = (uint32_t)(j >> 2) * 512 + (uint32_t)(r & 31) * 16 + (uint32_t)((r >> 5) & 3) * 4 +
+                                        (uint32_t)(j & 3);
+                asm volatile("st.shared.u8 [%0], %1;" ::"r"(sf_dst + sf_off), "r"(sf) : "memory");
+            }
+            fence_proxy_async_shared();                      // the MMA reads the A tile through the async proxy
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full[stage]);
+            if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+    }
+}
+
 // kMx: MXFP4 operands (one UE8M0 scale per 32 K-elements, two 512-byte scale
 // tiles per band and stage, scale_vec::2X MMAs); otherwise NVFP4 (one UE4M3
 // scale per 16 K-elements, four tiles per band and stage, scale_vec::4X).
-template <bool kMx>
+// kFused: the fused small-m linear (NVFP4, m <= kFusedMaxRows): no A tensor
+// is read; warp 0 quantizes each stage's slice of the activation p.quant.x
+// (the body of quant_kernel for the stage's 16 blocks of every row) straight
+// into the stage's A tile and scale tiles in shared memory.
+template <bool kMx, bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmOut, const GemmParams p)
+                     const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmX,
+                     const GemmParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -137,7 +255,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *mma_done = tmem_empty + 1;
     uint64_t *bias_full = mma_done + 1;     // [2]
     uint64_t *bias_empty = bias_full + 2;   // [2]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bias_empty + 2);
+    uint64_t *x_full = bias_empty + 2;      // [kStages] fused linear: the stage's activation slice landed
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(x_full + kStages);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -155,14 +274,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bias_full[b], 1);
             mbar_init(&bias_empty[b], kEpiWarps);
         }
+        if constexpr (kFused)
+            for (int s = 0; s < kStages; ++s) mbar_init(&x_full[s], 1);
         fence_mbarrier_init();
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
+        if constexpr (kFused) prefetch_tensormap(&tmX);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
+    if constexpr (kFused) quant_core::fill_inv_table(reinterpret_cast<float *>(smem + kOffInvTab), __ldg(p.quant.gs));
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -344,7 +467,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         setmaxnreg_dec<kRegsCtl>();
-        if ((warp == 0 || warp == 3) && lane == 0 && !p.drill) {   // (a timeout drill issues no copies)
+        if (kFused && warp == 0) {
+            if (!p.drill) fused_act_producer<kFused>(p, &tmX, smem, full, empty, x_full, num_ks, lane);
+        } else if ((warp == 0 || warp == 3) && lane == 0 && !p.drill) {   // (a timeout drill issues no copies)
             // ----------------------------------------------------- producers --
             // Two threads fill the ring, each with its half of every stage:
             // warp 0 the activation side (A tile + its scale tile), warp 3 the
@@ -358,7 +483,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool act_side = warp == 0;
             // weights are re-read by every 128-row band; with one band they stream once
             const uint64_t pol = act_side || p.num_m_blk > 1 ? l2_policy_evict_last() : l2_policy_evict_first();
-            if (act_side) griddep_wait();
+            // The fused linear, a programmatic dependent of an arbitrary
+            // kernel, waits on both sides: that kernel may write the weights.
+            if (act_side || kFused) griddep_wait();
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued_mask = 0, issued_phase = 0;
@@ -487,33 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const GemmParams p)
 {
     griddep_wait();                                 // the split GEMM's partials are complete
-    const float alpha = p.alpha != nullptr ? __ldg(p.alpha) : 1.0f;
-    const int groups = (p.n_out + 3) / 4;
-    const int64_t total = (int64_t)p.m * groups;
-    const int64_t split_stride = (int64_t)p.m * p.part_ld;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t r = i / groups;
-        const int c = (int)(i - r * groups) * 4;
-        const float *src = p.partials + r * p.part_ld + c;
-        // all loads in flight at once, then the sum in split order
-        float4 v[kMaxSplits];
-#pragma unroll
-        for (int sp = 0; sp < kMaxSplits; ++sp)
-            if (sp < p.splits) v[sp] = __ldcs(reinterpret_cast<const float4 *>(src + sp * split_stride));
-        float4 acc = v[0];
-#pragma unroll
-        for (int sp = 1; sp < kMaxSplits; ++sp)
-            if (sp < p.splits) { acc.x += v[sp].x; acc.y += v[sp].y; acc.z += v[sp].z; acc.w += v[sp].w; }
-        const float a[4] = {acc.x, acc.y, acc.z, acc.w};
-        uint16_t *o = p.out + r * p.ldo + c;
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            if (c + e < p.n_out) {
-                const float b = p.bias ? __uint_as_float((uint32_t)p.bias[c + e] << 16) : 0.0f;
-                o[e] = (uint16_t)bf16_bits_rn(__fmaf_rn(a[e], alpha, b));
-            }
-    }
+    reduce_partials(p, (int64_t)blockIdx.x * blockDim.x + threadIdx.x, (int64_t)gridDim.x * blockDim.x);
 }
 
 }  // namespace
@@ -537,17 +638,26 @@ cudaError_t launch_splitk_reduce(const GemmParams &p, int num_sms, cudaStream_t 
     return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, p);
 }
 
-cudaError_t launch_gemm(const GemmParams &p, const uint8_t *a, const uint8_t *w, int num_sms, cudaStream_t s,
-                        const char **why, bool dependent)
+namespace {
+
+// Launches the one-CTA kernel: the plain GEMM or, with `fused`, the fused
+// small-m linear, optionally as a programmatic dependent of the kernel before
+// it (only the activation side waits for that kernel; the weights stream at
+// once).
+cudaError_t launch_one_cta(const GemmParams &p, const uint8_t *a, const uint8_t *w, int num_sms, cudaStream_t s,
+                           const char **why, bool dependent, bool fused)
 {
     static int configured_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_nvf4_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(gemm_nvf4_kernel<false, false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(gemm_nvf4_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            e = cudaFuncSetAttribute(gemm_nvf4_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gemm_nvf4_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)kSmemBytes);
         if (e != cudaSuccess) return e;
         configured_device = dev;
@@ -579,8 +689,34 @@ cudaError_t launch_gemm(const GemmParams &p, const uint8_t *a, const uint8_t *w,
     cfg.stream = s;
     cfg.attrs = dependent ? &attr : nullptr;
     cfg.numAttrs = dependent ? 1 : 0;
-    return p.mx ? cudaLaunchKernelEx(&cfg, gemm_nvf4_kernel<true>, tmA, tmB, tmOut, p)
-                : cudaLaunchKernelEx(&cfg, gemm_nvf4_kernel<false>, tmA, tmB, tmOut, p);
+    CUtensorMap tmX = tmA;                              // the plain GEMM reads no bf16 activation
+    if (fused && !make_x_slice_map(&tmX, p.quant.x, (uint64_t)p.quant.k, (uint64_t)p.quant.m, (uint64_t)p.quant.ldx)) {
+        *why = "cuTensorMapEncodeTiled failed for the activation";
+        return cudaErrorInvalidValue;
+    }
+    if (fused) return cudaLaunchKernelEx(&cfg, gemm_nvf4_kernel<false, true>, tmA, tmB, tmOut, tmX, p);
+    return p.mx ? cudaLaunchKernelEx(&cfg, gemm_nvf4_kernel<true, false>, tmA, tmB, tmOut, tmX, p)
+                : cudaLaunchKernelEx(&cfg, gemm_nvf4_kernel<false, false>, tmA, tmB, tmOut, tmX, p);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmParams &p, const uint8_t *a, const uint8_t *w, int num_sms, cudaStream_t s,
+                        const char **why, bool dependent)
+{
+    return launch_one_cta(p, a, w, num_sms, s, why, dependent, false);
+}
+
+cudaError_t launch_linear_fused(const GemmParams &p, const uint8_t *w, int num_sms, cudaStream_t s, const char **why)
+{
+    if (p.mx || p.m > kFusedMaxRows || p.quant.bs != 0 || p.group_offsets != nullptr) {
+        *why = "the fused linear takes NVFP4 activations of at most 8 rows, without a transform";
+        return cudaErrorInvalidValue;
+    }
+    // A programmatic dependent of the kernel before it: the prologue (barrier
+    // set-up, TMEM allocation, scale table) overlaps that kernel's tail, and
+    // both producers wait for it before their first copy.
+    return launch_one_cta(p, p.quant.out, w, num_sms, s, why, true, true);
 }
 
 }  // namespace nvfp4

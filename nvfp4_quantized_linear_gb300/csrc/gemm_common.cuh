@@ -128,6 +128,22 @@ inline bool make_scale_bands_map(CUtensorMap *map, const void *base, uint64_t ba
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Map of a bf16 activation [m, k] (row stride ld elements) for copies of 256
+// columns x 16 rows (the fused small-m linear's per-stage slice), no swizzle,
+// zero fill past m and k.  Requires a 16-B aligned base and ld % 8 == 0.
+inline bool make_x_slice_map(CUtensorMap *map, const void *base, uint64_t k, uint64_t m, uint64_t ld)
+{
+    auto encode = tensor_map_encoder();
+    if (encode == nullptr) return false;
+    cuuint64_t dims[2] = {k, m};
+    cuuint64_t strides[1] = {ld * 2};
+    cuuint32_t box[2] = {256, 16};
+    cuuint32_t estr[2] = {1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D map over bf16 rows [rows, cols] (row stride ld elements) with boxes of
 // 64 columns x 128 rows, 128-byte swizzle (the K-major operand layout of a
 // kind::f16 MMA), zero fill outside the tensor.  Requires a 16-B aligned base
