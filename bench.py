@@ -698,7 +698,7 @@ def run_suite(args, dev):
     from nvfp4_quantized_linear_gb300 import synthetic as syn
     nv.build()
     peaks, _ = load_peaks()
-    fp4_peak = peaks["bf16_tflops_sustained"] * FP4_OVER_BF16
+    fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16          # burst: each kernel is timed alone
     hbm = peaks["hbm_gbs"]
     stream = torch.cuda.current_stream().cuda_stream
     timed = _cold_timer(torch, dev)
@@ -776,6 +776,54 @@ def run_suite(args, dev):
                "note": "amax pass (read of x, memset and finalize launches included), then the quantizer"}
         del x, x_fp4, x_sf
         torch.cuda.empty_cache()
+
+    # MXFP4 GEMM and linear on the largest layers of the Llama and Qwen
+    # workloads (operands quantized by the MXFP4 quantizer, no alpha)
+    for p in [q for q in syn.llama([8192]) + syn.qwen([16384]) if q.name in ("gate_up", "down")]:
+        x = syn.make_activation(p, device=dev)
+        w = syn.bf16_normal((p.n, p.k), 0.02, p.seed + 100_000, device=dev)
+        a_fp4, a_sf = nv.quant_act_mx(x)
+        w_fp4, w_sf = nv.quant_act_mx(w)
+        del w
+        out = torch.empty((p.m, p.n), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(nv.nvfp4_mxfp4_linear_workspace_bytes(p.m, p.k, p.n), dtype=torch.uint8, device=dev)
+        tg = timed(lambda: nv.nvfp4_mxfp4_gemm(a_fp4, a_sf, p.m, w_fp4, w_sf, p.n, p.n, p.k, None, out, p.n, stream))
+        tl = timed(lambda: nv.nvfp4_mxfp4_linear(x, p.m, p.k, p.k, w_fp4, w_sf, p.n, p.n, None, out, p.n, ws,
+                                                 ws.numel(), stream))
+        nv.nvfp4_device_error()
+        yield {"suite": "mxfp4_gemm", "workload": p.workload, "layer": p.name, "m": p.m, "k": p.k, "n": p.n,
+               "gemm_us": round(tg * 1e6, 2), "gemm_tflops": round(p.flops / tg / 1e12, 1),
+               "gemm_frac_fp4": round(p.flops / tg / 1e12 / fp4_peak, 4),
+               "linear_us": round(tl * 1e6, 2), "linear_tflops": round(p.flops / tl / 1e12, 1)}
+        del x, a_fp4, a_sf, w_fp4, w_sf, out, ws
+        torch.cuda.empty_cache()
+
+    # grouped (mixture-of-experts) GEMM: 8 experts, about 1000 tokens each
+    # (a prefill batch routed top-2), K = 4096 -> N = 2 x 14336 / 8 per expert
+    group_m = [1000, 1200, 880, 1024, 1111, 960, 1030, 990]
+    gk, gn = 4096, 3584
+    offs = [0]
+    for gm in group_m:
+        offs.append(offs[-1] + (gm + 127) // 128 * 128)
+    rows = offs[-1]
+    x = syn.bf16_normal((rows, gk), 1.0, 4900, device=dev)
+    w = syn.bf16_normal((len(group_m) * gn, gk), 0.02, 4901, device=dev)
+    a_fp4, a_sf = nv.quant_act(x, torch.tensor([30.0], **f32))
+    w_fp4, w_sf = nv.prepare_weight(w, torch.tensor([syn.global_scale(w)], **f32))
+    del w
+    offsets = torch.tensor(offs, dtype=torch.int32, device=dev)
+    alphas = torch.full((len(group_m),), 1e-3, **f32)
+    out = torch.empty((rows, gn), dtype=torch.bfloat16, device=dev)
+    tg = timed(lambda: nv.nvfp4_grouped_gemm(a_fp4, a_sf, rows, offsets, len(group_m), w_fp4, w_sf, gn, gk, alphas,
+                                             None, out, gn, stream))
+    nv.nvfp4_device_error()
+    flops = 2 * sum(group_m) * gn * gk
+    yield {"suite": "grouped_gemm", "groups": len(group_m), "tokens": sum(group_m), "rows_padded": rows, "k": gk,
+           "n": gn, "gemm_us": round(tg * 1e6, 2), "tflops": round(flops / tg / 1e12, 1),
+           "frac_fp4": round(flops / tg / 1e12 / fp4_peak, 4),
+           "note": "FLOPs of the real tokens; the padding rows of each group's last band are computed too"}
+    del x, a_fp4, a_sf, w_fp4, w_sf, out
+    torch.cuda.empty_cache()
 
     # MXFP4 activation quantization (block 32, E8M0 scales, no global scale)
     for m, k in [(8192, 4096), (8192, 14336), (65536, 16384)]:
