@@ -20,21 +20,23 @@ struct Tile {
 template <bool kMx>
 constexpr int kSfTilesPerStage = kMx ? 2 : 4;
 
-// Tiles are walked column by column (row band fastest) inside groups of up to
-// 64 row bands: the CTAs resident at one time work on a few weight column
-// bands, so each weight tile is streamed from DRAM about once and shared by
-// the row bands through L2, while the group's activation rows (at most 64
-// bands) stay resident in L2 across columns.
-constexpr int kTileGroupBands = 64;   // row bands per group of the tile walk
-
-__device__ __forceinline__ Tile tile_coord(int tile, int num_m, int num_n)
+// Tiles are walked column by column (row band fastest) inside groups of
+// `group` row bands (at most): the CTAs resident at one time work on a few
+// weight column bands, so each weight tile is streamed from DRAM about once
+// and shared by the row bands through L2, while the group's activation rows
+// stay resident in L2 across columns.  Both GEMM kernels use groups of 8192
+// activation rows (64 bands of 128 rows, or 32 pair tiles of 256 rows): on the
+// Qwen gate_up shape (M = 16384, K = 5120) the CTA-pair kernel measured
+// 1278 us with 32-tile groups against 1327 us with 64 and 1311 / 1385 us with
+// 16 / 8.
+__device__ __forceinline__ Tile tile_coord(int tile, int num_m, int num_n, int group = 64)
 {
-    const int G = num_m < kTileGroupBands ? num_m : kTileGroupBands;
+    const int G = num_m < group ? num_m : group;
     const int per_group = G * num_n;
-    const int group = tile / per_group;
-    const int first_m = group * G;
+    const int grp = tile / per_group;
+    const int first_m = grp * G;
     const int gm = min(G, num_m - first_m);
-    const int within = tile - group * per_group;
+    const int within = tile - grp * per_group;
     return {first_m + within % gm, within / gm};
 }
 

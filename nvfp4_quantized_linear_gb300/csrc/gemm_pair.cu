@@ -4,25 +4,28 @@
 // section 关键源码片段: _scaled_mm, * alpha, slice, + bias), with each output
 // tile of 256 x 256 computed by a cluster of two CTAs on two SMs.  Per CTA
 // r (r = 0, 1; rank 0 leads), sixteen warps in four warpgroups:
-//   warps 0, 3  TMA producers: warp 0 this CTA's A rows [128r, 128r + 128) of
-//               the tile and their scale tile, warp 3 its half of B (rows
-//               [128r, 128r + 128) of the tile's 256) and the scale tiles of
-//               both B bands (each CTA's TMEM needs the scales of all 256 B
-//               rows), into a 5-stage ring of 38 KB stages;
+//   warps 0, 3  TMA producers of the operand ring (5 stages of 32 KB): warp 0
+//               this CTA's A rows [128r, 128r + 128) of the tile, warp 3 its
+//               half of B (rows [128r, 128r + 128) of the tile's 256);
+//   warp 2      TMA producer of the scale ring (5 stages of 6 KB): this CTA's
+//               A scale band and the scale tiles of both B bands (each CTA's
+//               TMEM needs the scales of all 256 B rows);
 //   warp 1      allocates the pair's TMEM; in the leader it issues, from one
 //               elected lane of the converged warp, tcgen05.mma.cta_group::2
 //               (M = 256, N = 256, K = 64): each CTA's tensor core reads its
 //               own A rows and both B halves and accumulates its 128 x 256
 //               fp32 tile in its own TMEM; the commits multicast to both CTAs'
 //               barriers;
-//   warp 2      loads each tile's bias into shared memory (two buffers);
-//   warps 4..7  stage each landed stage's scale tiles into this CTA's TMEM
-//               (tcgen05.st, one warp per lane quarter) and arrive on the
-//               leader's sf_ready[stage], which therefore completes once both
-//               CTAs' stages landed and both TMEMs hold their scales;
-//   warps 8..15 epilogue, two per TMEM lane quarter: drain this CTA's
-//               accumulator (alpha, bias, bf16), arrive on the leader's
-//               accumulator-free barrier, then TMA-store the rows.
+//   warps 4..7  one per TMEM lane quarter: read a stage's scales from the
+//               scale ring (and release it), write them into the stage's TMEM
+//               columns once the MMAs of the slot's previous use are done
+//               (tcgen05.st), wait for the stage's operands in this CTA and
+//               arrive on the leader's sf_ready[stage], which therefore
+//               completes once both CTAs hold the stage's operands and scales;
+//   warps 8..15 epilogue, two per TMEM lane quarter: load this CTA's whole
+//               accumulator into registers (four loads in flight), hand it
+//               back to the MMA warp, then apply alpha and bias, round to bf16
+//               and TMA-store the rows.
 // Per SM and stage this moves 38 KB into shared memory instead of 54 KB, so
 // five stages fit where the one-CTA kernel holds four.  Every mbarrier wait is
 // bounded; all threads meet at one final cluster barrier before the TMEM is
@@ -39,10 +42,12 @@ namespace {
 using namespace gemm_detail;
 
 constexpr int kTileM = 256;                     // per pair (128 rows per CTA)
+constexpr int kWalkGroup = 32;                  // pair tiles per group of the tile walk (8192 rows)
 constexpr int kTileN = 256;
 constexpr int kRowsCta = 128;
 constexpr int kBKBytes = 128;                   // 256 FP4 elements of K per stage
 constexpr int kStages = 5;
+constexpr int kEpiColsBias = 128;                     // bias columns per epilogue warp
 constexpr uint32_t kABytes = kRowsCta * kBKBytes;     // 16 KB: this CTA's A rows
 constexpr uint32_t kBBytes = kRowsCta * kBKBytes;     // 16 KB: this CTA's half of B
 constexpr uint32_t kSfaBytes = 4 * 512;               // this CTA's A band, 4 K-steps
@@ -52,8 +57,8 @@ constexpr uint32_t kOffA = 0;
 constexpr uint32_t kOffB = kOffA + kStages * kABytes;
 constexpr uint32_t kOffSfa = kOffB + kStages * kBBytes;
 constexpr uint32_t kOffSfb = kOffSfa + kStages * kSfaBytes;
-constexpr uint32_t kOffBias = kOffSfb + kStages * kSfbBytes;  // two tiles of bias (bf16)
-constexpr uint32_t kOffOut = (kOffBias + 2 * kTileN * 2 + 1023) / 1024 * 1024;   // one chunk per epilogue warp
+constexpr uint32_t kOffBias = kOffSfb + kStages * kSfbBytes;  // per epilogue warp: its 128 bias columns (bf16)
+constexpr uint32_t kOffOut = (kOffBias + 8 * kEpiColsBias * 2 + 1023) / 1024 * 1024;   // one chunk per epilogue warp
 constexpr uint32_t kOffBar = kOffOut + 8 * kOutChunkBytes;
 constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;         // barriers + alignment slack
 constexpr uint32_t kTmemCols = 512;
@@ -65,7 +70,9 @@ constexpr int kEpiWarp0 = 8;
 constexpr int kEpiWarps = 8;
 constexpr int kEpiCols = kTileN / 2;
 constexpr uint16_t kBothCtas = 0x3;
-constexpr uint32_t kRegsCtl = 56, kRegsSf = 96, kRegsEpi = 176;
+// registers per thread after setmaxnreg: the epilogue holds a whole 128-column
+// accumulator slice (128 registers) at once
+constexpr uint32_t kRegsCtl = 56, kRegsSf = 88, kRegsEpi = 184;
 
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffOut % 1024 == 0, "128-byte-swizzled TMA store sources are 1024-byte aligned");
@@ -81,15 +88,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kOffBar);   // this CTA's stage landed
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kOffBar);   // this CTA's operands of the stage landed
     uint64_t *empty = full + kStages;                                 // the pair's MMAs released the stage
     uint64_t *sf_ready = empty + kStages;                             // (leader) both CTAs' scales staged
     uint64_t *tmem_full = sf_ready + kStages;                         // accumulator complete
     uint64_t *tmem_empty = tmem_full + 1;                             // (leader) both CTAs drained it
     uint64_t *mma_done = tmem_empty + 1;
-    uint64_t *bias_full = mma_done + 1;                               // [2]
-    uint64_t *bias_empty = bias_full + 2;                             // [2]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bias_empty + 2);
+    uint64_t *sf_full = mma_done + 1;                                 // the stage's scale tiles landed
+    uint64_t *sf_empty = sf_full + kStages;                           // the scale warps have read them
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sf_empty + kStages);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -105,9 +112,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(tmem_full, 1);
         mbar_init(tmem_empty, 2 * kEpiWarps);
         mbar_init(mma_done, 1);
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&bias_full[b], 1);
-            mbar_init(&bias_empty[b], kEpiWarps);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&sf_full[s], 1);          // the scale producer
+            mbar_init(&sf_empty[s], 4);         // the four scale warps
         }
         fence_mbarrier_init();
         prefetch_tensormap(&tmA);
@@ -139,69 +146,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t out_stage = smem_u32(smem + kOffOut) + (warp - kEpiWarp0) * kOutChunkBytes;
         const uint32_t leader_tmem_empty = mapa_shared(tmem_empty, 0);
         const bool use_bias = p.bias != nullptr;
+        const bool bias_vec = (reinterpret_cast<uintptr_t>(p.bias) & 7) == 0;   // 8-byte loads of 4 columns
         const float alpha = p.alpha != nullptr ? __ldg(p.alpha) : 1.0f;
         const uint64_t out_policy = l2_policy_evict_first();   // the output is written once
         uint32_t acc_phase = 0;
         int it = 0;
         for (int tile = pair_id; tile < num_tiles; tile += num_pairs, ++it) {
-            const Tile t = tile_coord(tile, p.num_m_blk, p.num_n_blk);
+            const Tile t = tile_coord(tile, p.num_m_blk, p.num_n_blk, kWalkGroup);
             const int n_cols = min(kEpiCols, p.n_out - t.nb * kTileN - hcol);   // may be <= 0
             const int col_base = t.nb * kTileN + hcol;
-            const uint16_t *s_bias = reinterpret_cast<const uint16_t *>(smem + kOffBias) + (it & 1) * kTileN + hcol;
-            if (use_bias &&
-                !__all_sync(~0u, mbar_wait(&bias_full[it & 1], (it >> 1) & 1, p.err_flag, kErrTimeout, p.wait_ns)))
-                break;
+            // this warp's 128 bias columns into its own buffer (four per lane)
+            // while the accumulator is still being computed
+            uint16_t *s_bias = reinterpret_cast<uint16_t *>(smem + kOffBias) + (warp - kEpiWarp0) * kEpiColsBias;
+            if (use_bias) {
+                const int c0 = col_base + 4 * lane;
+                uint2 bw = make_uint2(0u, 0u);
+                if (bias_vec && c0 + 4 <= p.n_out) {
+                    bw = __ldg(reinterpret_cast<const uint2 *>(p.bias + c0));
+                } else {
+                    uint16_t e[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) e[i] = (c0 + i < p.n_out) ? p.bias[c0 + i] : (uint16_t)0;
+                    bw = make_uint2(e[0] | ((uint32_t)e[1] << 16), e[2] | ((uint32_t)e[3] << 16));
+                }
+                *reinterpret_cast<uint2 *>(s_bias + 4 * lane) = bw;
+                __syncwarp();
+            }
             if (!__all_sync(~0u, mbar_wait(tmem_full, acc_phase, p.err_flag, kErrTimeout, p.wait_ns))) break;
             tc_fence_after_sync();
             acc_phase ^= 1;
 
-            // Drain this warp's 128 accumulator columns in four 32-column
-            // loads, double-buffered: the next load is in flight while the
-            // current chunk gets alpha and bias and is rounded.  The
-            // accumulator goes back to the MMA warp right after the last load
-            // has landed, before that chunk's arithmetic.
-            uint32_t r0[32], r1[32];
-            uint32_t packed[kEpiCols / 2];
-            if (n_cols > 0) tmem_ld_32cols(acc, r0);
+            // Load this warp's 128 accumulator columns with all four 32-column
+            // loads in flight and hand the accumulator back to the MMA warp
+            // as soon as they have landed: the next tile's MMAs wait only for
+            // the loads, not for the arithmetic and stores below.
+            uint32_t acc_regs[kEpiCols / 32][32];
+            if (n_cols > 0) {                                   // uniform across the warp
 #pragma unroll
-            for (int ch = 0; ch < kEpiCols / 32; ++ch) {
-                uint32_t(&cur)[32] = (ch & 1) ? r1 : r0;
-                uint32_t(&nxt)[32] = (ch & 1) ? r0 : r1;
-                if (n_cols > 0) {                               // uniform across the warp
-                    tmem_ld_wait_regs(cur);
-                    if (ch + 1 < kEpiCols / 32) tmem_ld_32cols(acc + (ch + 1) * 32, nxt);
-                }
-                if (ch + 1 == kEpiCols / 32) {
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (is_leader) mbar_arrive(tmem_empty);  // the leader's own barrier: local arrive
-                        else mbar_arrive_remote(leader_tmem_empty);
-                    }
-                }
-                if (ch * 32 < n_cols) {                         // uniform across the warp
+                for (int ch = 0; ch < kEpiCols / 32; ++ch) tmem_ld_32cols(acc + ch * 32, acc_regs[ch]);
 #pragma unroll
-                    for (int j = 0; j < 32; j += 2) {
-                        float b0 = 0.0f, b1 = 0.0f;
-                        if (use_bias) {
-                            const uint32_t bw = *reinterpret_cast<const uint32_t *>(s_bias + ch * 32 + j);
-                            b0 = __uint_as_float(bw << 16);
-                            b1 = __uint_as_float(bw & 0xFFFF0000u);
-                        }
-                        packed[ch * 16 + j / 2] = bf16x2_rn(__fmaf_rn(__uint_as_float(cur[j]), alpha, b0),
-                                                            __fmaf_rn(__uint_as_float(cur[j + 1]), alpha, b1));
-                    }
-                }
+                for (int ch = 0; ch < kEpiCols / 32; ++ch) tmem_ld_wait_regs(acc_regs[ch]);
             }
-            if (use_bias) {
-                __syncwarp();                                   // every lane has read the bias buffer
-                if (lane == 0) mbar_arrive(&bias_empty[it & 1]);
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                if (is_leader) mbar_arrive(tmem_empty);          // the leader's own barrier: local arrive
+                else mbar_arrive_remote(leader_tmem_empty);
             }
 
-            // TMA stores of two 32-row x 64-column chunks (128-byte rows, the
-            // TMA's 128-byte swizzle: 16-byte piece j of row r sits at piece
-            // j ^ (r % 8), which also spreads the 32 lanes' writes over all
-            // banks) through this warp's staging buffer; rows >= m and
+            // alpha, bias and bf16 rounding, 32 columns at a time, straight
+            // into this warp's staging buffer; then TMA stores of two 32-row
+            // x 64-column chunks (128-byte rows, the TMA's 128-byte swizzle:
+            // 16-byte piece j of row r sits at piece j ^ (r % 8), which also
+            // spreads the 32 lanes' writes over all banks).  Rows >= m and
             // columns >= n_out are clipped by the TMA.
             const int row0 = t.mb * kTileM + (int)rank * kRowsCta + q * 32;
 #pragma unroll
@@ -210,9 +207,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) bulk_wait_group_read<0>();   // the previous store has read the buffer
                     __syncwarp();
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        st_shared_v4(out_stage + lane * 128 + ((j ^ (lane & 7)) << 4), packed[c * 32 + j * 4],
-                                     packed[c * 32 + j * 4 + 1], packed[c * 32 + j * 4 + 2], packed[c * 32 + j * 4 + 3]);
+                    for (int h = 0; h < 2; ++h) {
+                        const int ch = c * 2 + h;
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int j = 0; j < 32; j += 2) {
+                            float b0 = 0.0f, b1 = 0.0f;
+                            if (use_bias) {
+                                const uint32_t bw = *reinterpret_cast<const uint32_t *>(s_bias + ch * 32 + j);
+                                b0 = __uint_as_float(bw << 16);
+                                b1 = __uint_as_float(bw & 0xFFFF0000u);
+                            }
+                            pk[j / 2] = bf16x2_rn(__fmaf_rn(__uint_as_float(acc_regs[ch][j]), alpha, b0),
+                                                  __fmaf_rn(__uint_as_float(acc_regs[ch][j + 1]), alpha, b1));
+                        }
+#pragma unroll
+                        for (int j4 = 0; j4 < 4; ++j4) {
+                            const int piece = h * 4 + j4;
+                            st_shared_v4(out_stage + lane * 128 + ((piece ^ (lane & 7)) << 4), pk[j4 * 4],
+                                         pk[j4 * 4 + 1], pk[j4 * 4 + 2], pk[j4 * 4 + 3]);
+                        }
+                    }
                     fence_proxy_async_shared();
                     __syncwarp();
                     if (lane == 0) {
@@ -221,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            __syncwarp();                                       // every lane has read the bias buffer
         }
         if (lane == 0) bulk_wait_group<0>();                    // all output written before the CTA exits
     } else if (warp >= kSfWarp0) {
@@ -228,8 +244,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ----------------------------------------------- scale staging --
         // tcgen05.cp 32x128b.warpx4 layout: lane 32q + i of quarter q gets
         // bytes [16i, 16i + 16) of each 512-byte scale tile.  A stage's TMEM
-        // columns are rewritten only after the stage landed again, i.e. after
-        // the MMAs that read them completed and released it.
+        // scale columns are rewritten only after the MMAs of its previous use
+        // have completed (their commit on `empty`).
         const int q = warp & 3;
         const uint32_t sf_tmem = tmem + ((uint32_t)(q * 32) << 16) + kTmemSf;
         const uint32_t sfa_smem = smem_u32(smem + kOffSfa) + lane * 16;
@@ -240,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int tile = pair_id; tile < num_tiles && ok; tile += num_pairs) {
             for (int ks = 0; ks < num_ks; ++ks) {
-                ok = __all_sync(~0u, mbar_wait(&full[stage], phase, p.err_flag, kErrTimeout, p.wait_ns));
+                ok = __all_sync(~0u, mbar_wait(&sf_full[stage], phase, p.err_flag, kErrTimeout, p.wait_ns));
                 if (!ok) break;
                 constexpr int kT = kSfTilesPerStage<kMx>;
                 uint32_t a[4 * kT], b[8 * kT];
@@ -257,6 +273,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint32_t *d = b + j * 8 + h * 4;
                         d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
                     }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sf_empty[stage]);   // the scale slot may be refilled
+                // The stage's TMEM scale columns are free once the MMAs of the
+                // slot's previous use are done (the commit on `empty`).
+                ok = __all_sync(~0u, mbar_wait(&empty[stage], phase ^ 1, p.err_flag, kErrTimeout, p.wait_ns));
+                if (!ok) break;
                 // (tiles past the valid K-steps, B rows or A rows hold stale
                 // bytes; what they meet in the MMA is never stored)
                 if constexpr (kMx) {
@@ -268,6 +290,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_st_wait();
                 tc_fence_before_sync();
+                // and this CTA's operands of the stage have landed: then the
+                // leader's MMA may read them (sf_ready counts both CTAs)
+                ok = __all_sync(~0u, mbar_wait(&full[stage], phase, p.err_flag, kErrTimeout, p.wait_ns));
+                if (!ok) break;
                 __syncwarp();
                 if (lane == 0) {
                     if (is_leader) mbar_arrive(&sf_ready[stage]);      // the leader's own barrier: local arrive
@@ -279,12 +305,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         setmaxnreg_dec<kRegsCtl>();
         if ((warp == 0 || warp == 3) && lane == 0 && !p.drill) {   // (a timeout drill issues no copies)
-            // ----------------------------------------------------- producers --
-            // Two threads per CTA fill the ring, each with its half of every
-            // stage and one arrival on `full` (count 2): warp 0 this CTA's A
-            // rows and their scale tile (after the wait for the preceding
-            // grid, the activation quantizer when launched as its dependent),
-            // warp 3 this CTA's half of B and the scale tiles of both B bands.
+            // ---------------------------------------------- operand producers --
+            // Two threads per CTA fill the operand ring, each with its half of
+            // every stage and one arrival on `full` (count 2): warp 0 this
+            // CTA's A rows (after the wait for the preceding grid, the
+            // activation quantizer when launched as its dependent), warp 3
+            // this CTA's half of B.
             const bool act_side = warp == 0;
             const uint64_t pol = l2_policy_evict_last();
             if (act_side) griddep_wait();
@@ -293,33 +319,63 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t issued_mask = 0, issued_phase = 0;
             bool ok = true;
             for (int tile = pair_id; tile < num_tiles && ok; tile += num_pairs) {
-                const Tile t = tile_coord(tile, p.num_m_blk, p.num_n_blk);
+                const Tile t = tile_coord(tile, p.num_m_blk, p.num_n_blk, kWalkGroup);
                 const int band_a = t.mb * 2 + (int)rank;
-                const bool a_here = band_a < a_bands;
                 for (int ks = 0; ks < num_ks; ++ks) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, p.err_flag, kErrTimeout, p.wait_ns)) {
                         ok = false;
                         break;
                     }
-                    constexpr int kT = kSfTilesPerStage<kMx>;
-                    const uint32_t sf_bytes = (uint32_t)min(kT, p.sf_tiles - ks * kT) * 512;
-                    if (act_side) {
-                        mbar_arrive_expect_tx(&full[stage], kABytes + (a_here ? sf_bytes : 0));
-                        tma_load_2d(smem + kOffA + stage * kABytes, &tmA, &full[stage], ks * kBKBytes, band_a * kRowsCta,
-                                    pol);
-                        if (a_here)
-                            bulk_load(smem + kOffSfa + stage * kSfaBytes,
-                                      p.sfa + band_a * p.sfa_band_bytes + (int64_t)ks * kT * 512, sf_bytes, &full[stage], pol);
-                    } else {
-                        // the stage's scale tiles of both B bands in one 2-D copy
-                        // (8-byte elements: box of kT tiles x 2 bands; past the
-                        // last band or K-step the TMA fills zeros)
-                        mbar_arrive_expect_tx(&full[stage], kBBytes + 2 * kT * 512);
+                    // (a box past the last row is zero-filled and still counts
+                    // its full bytes)
+                    mbar_arrive_expect_tx(&full[stage], act_side ? kABytes : kBBytes);
+                    if (act_side)
+                        tma_load_2d(smem + kOffA + stage * kABytes, &tmA, &full[stage], ks * kBKBytes,
+                                    band_a * kRowsCta, pol);
+                    else
                         tma_load_2d(smem + kOffB + stage * kBBytes, &tmB, &full[stage], ks * kBKBytes,
                                     t.nb * kTileN + (int)rank * kRowsCta, pol);
-                        tma_load_2d(smem + kOffSfb + stage * kSfbBytes, &tmSfb, &full[stage], ks * kT * 64, t.nb * 2,
-                                    pol);
+                    issued_mask |= 1u << stage;
+                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == kStages) { stage = 0; phase ^= 1; }
+                }
+            }
+            for (int s = 0; s < kStages; ++s)
+                    if (issued_mask & (1u << s))
+                    mbar_wait(&full[s], (issued_phase >> s) & 1u, p.err_flag, kErrTimeout, p.wait_ns);
+        } else if (warp == 2 && lane == 0 && !p.drill) {
+            // ------------------------------------------------- scale producer --
+            // The scale tiles travel apart from the operands, in a ring of
+            // their own that frees as soon as the scale warps have read it:
+            // so they are requested stages ahead, and a stage's scales are in
+            // TMEM before its operands land.  Per stage: this CTA's A band
+            // (kT tiles, bulk copy) and both B bands of the tile (one 2-D copy,
+            // 8-byte elements, box of kT tiles x 2 bands; the TMA fills zeros
+            // past the last band or K-step).  The A scales may be the
+            // preceding grid's output (the quantizer): wait for it first.
+            constexpr int kT = kSfTilesPerStage<kMx>;
+            const uint64_t pol = l2_policy_evict_last();
+            griddep_wait();
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_mask = 0, issued_phase = 0;
+            bool ok = true;
+            for (int tile = pair_id; tile < num_tiles && ok; tile += num_pairs) {
+                const Tile t = tile_coord(tile, p.num_m_blk, p.num_n_blk, kWalkGroup);
+                const int band_a = t.mb * 2 + (int)rank;
+                const bool a_here = band_a < a_bands;
+                for (int ks = 0; ks < num_ks; ++ks) {
+                    if (!mbar_wait(&sf_empty[stage], phase ^ 1, p.err_flag, kErrTimeout, p.wait_ns)) {
+                        ok = false;
+                        break;
                     }
+                    const uint32_t sfa_bytes = (uint32_t)min(kT, p.sf_tiles - ks * kT) * 512;
+                    mbar_arrive_expect_tx(&sf_full[stage], (a_here ? sfa_bytes : 0) + 2 * kT * 512);
+                    if (a_here)
+                        bulk_load(smem + kOffSfa + stage * kSfaBytes,
+                                  p.sfa + band_a * p.sfa_band_bytes + (int64_t)ks * kT * 512, sfa_bytes, &sf_full[stage],
+                                  pol);
+                    tma_load_2d(smem + kOffSfb + stage * kSfbBytes, &tmSfb, &sf_full[stage], ks * kT * 64, t.nb * 2, pol);
                     issued_mask |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == kStages) { stage = 0; phase ^= 1; }
@@ -327,23 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             for (int s = 0; s < kStages; ++s)
                 if (issued_mask & (1u << s))
-                    mbar_wait(&full[s], (issued_phase >> s) & 1u, p.err_flag, kErrTimeout, p.wait_ns);
-        } else if (warp == 2 && p.bias != nullptr) {
-            // ---------------------------------------------------- bias loader --
-            uint16_t *s_bias_all = reinterpret_cast<uint16_t *>(smem + kOffBias);
-            int it = 0;
-            for (int tile = pair_id; tile < num_tiles; tile += num_pairs, ++it) {
-                const Tile t = tile_coord(tile, p.num_m_blk, p.num_n_blk);
-                const int n_rows = min(kTileN, p.n_out - t.nb * kTileN);
-                const int b = it & 1;
-                if (!__all_sync(~0u, mbar_wait(&bias_empty[b], ((it >> 1) & 1) ^ 1, p.err_flag, kErrTimeout,
-                                               p.wait_ns)))
-                    break;
-                for (int j = lane; j < kTileN; j += 32)
-                    s_bias_all[b * kTileN + j] = (j < n_rows) ? p.bias[t.nb * kTileN + j] : (uint16_t)0;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bias_full[b]);
-            }
+                    mbar_wait(&sf_full[s], (issued_phase >> s) & 1u, p.err_flag, kErrTimeout, p.wait_ns);
         } else if (warp == 1 && is_leader) {
             // ---------------------------------------------------- MMA (leader) --
             // The whole warp runs the loop (warp-uniform values); one elected
@@ -360,6 +400,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 tc_fence_after_sync();
                 for (int ks = 0; ks < num_ks; ++ks) {
+                    // the stage's scales in both CTAs' TMEM, its operands in both
+                    // CTAs' shared memory
                     if (!__all_sync(~0u, mbar_wait(&sf_ready[stage], phase, p.err_flag, kErrTimeout, p.wait_ns))) {
                         ok = false;
                         break;

@@ -464,7 +464,6 @@ __device__ __forceinline__ uint32_t mapa_shared(const void *local, uint32_t rank
     return r;
 }
 
-// Arrive (release at cluster scope) on an mbarrier given by its shared::cluster address.
 // Arrive on an mbarrier of a CTA of this cluster (shared::cluster address from
 // mapa) with the instruction's default semantics (release, CTA scope): the
 // arrival is performed at the barrier's CTA.  Much cheaper than a
@@ -474,6 +473,7 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// Arrive (release at cluster scope) on an mbarrier given by its shared::cluster address.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
 {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
