@@ -114,10 +114,8 @@ size_t nvfp4_packed_bytes(int64_t rows, int64_t k);
 size_t nvfp4_scale_bytes(int64_t rows, int64_t k);
 
 /* Workspace nvfp4_linear wants for an m x k activation against n_w weight
- * rows: the quantized activation and its scales (each 256-B aligned inside)
- * and, for m <= 128, room for split-K partial sums (640 * 256 fp32 per row).
- * nvfp4_linear accepts any workspace that holds the first two; given less than
- * this size, a small-m call runs without split-K. */
+ * rows: the quantized activation and its scales, each 256-B aligned inside
+ * (n_w is accepted for future use and does not change the size). */
 size_t nvfp4_linear_workspace_bytes(int64_t m, int64_t k, int64_t n_w);
 
 /* ---- operations ---------------------------------------------------------- */
@@ -203,7 +201,7 @@ nvfp4_status nvfp4_mxfp4_gemm(const uint8_t *a_fp4, const uint8_t *a_sf, int64_t
  * nvfp4_mxfp4_quant_act of x into `workspace`, then nvfp4_mxfp4_gemm, on one
  * stream.  workspace: caller-owned device scratch of at least
  * align256(nvfp4_packed_bytes(m,k)) + align256(nvfp4_mxfp4_scale_bytes(m,k))
- * bytes; with nvfp4_mxfp4_linear_workspace_bytes and m <= 128 the GEMM may
+ * bytes (= nvfp4_mxfp4_linear_workspace_bytes); with m <= 128 the GEMM may
  * split K as nvfp4_linear does. */
 size_t nvfp4_mxfp4_linear_workspace_bytes(int64_t m, int64_t k, int64_t n_w);
 nvfp4_status nvfp4_mxfp4_linear(const void *x_bf16, int64_t m, int64_t k, int64_t ldx,
@@ -253,7 +251,9 @@ nvfp4_status nvfp4_gemm(const uint8_t *a_fp4, const uint8_t *a_sf, int64_t m,
  * testing its kernels and its failure path (the pages have no counterpart):
  *   kernel         0: as nvfp4_gemm (the CTA-pair kernel for m > 128, else the
  *                     one-CTA kernel);  1: the one-CTA kernel at any m;
- *                  2: the CTA-pair kernel (m > 128 only, else NVFP4_ERR_INVALID_ARG).
+ *                  2: the CTA-pair kernel (m > 128 only, else NVFP4_ERR_INVALID_ARG);
+ *                  3: the one-CTA kernel with nvfp4_linear's split-K plan
+ *                     (m <= 128 splits as nvfp4_linear would).
  *   wait_limit_ns  bound of every pipeline barrier wait of this launch, in
  *                  [1e6, 1e10] ns; 0 = the library's two seconds.
  *   drill          0: compute normally.  1: timeout drill -- the kernel's copy
@@ -307,12 +307,13 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t *a_fp4, const uint8_t *a_sf, int64
  * the GEMM of nvfp4_gemm, all on `stream`.  workspace (device) is scratch owned
  * by the caller, at least align256(nvfp4_packed_bytes(m,k)) +
  * align256(nvfp4_scale_bytes(m,k)) bytes (else NVFP4_ERR_WORKSPACE); its
- * contents after the call are unspecified.  With m <= 128 and a workspace of
- * nvfp4_linear_workspace_bytes, a GEMM whose output has too few 128 x 256
- * tiles to fill the GPU splits K across CTAs: each writes fp32 partial sums to
- * the workspace and a second kernel adds them in split order, then applies
- * alpha and bias.  The result is deterministic, but its fp32 rounding order
- * differs from the unsplit GEMM's (both are within the GEMM's accuracy).
+ * contents after the call are unspecified.  With m <= 128, a GEMM whose
+ * output has too few 128 x 256 tiles to fill the GPU splits K: the K ranges
+ * of a tile run as the CTAs of one thread-block cluster, which add their fp32
+ * partial sums through distributed shared memory in range order before alpha,
+ * bias and the bf16 rounding (no extra launch, no partials in memory).  The
+ * result is deterministic, but its fp32 rounding order differs from the
+ * unsplit GEMM's (both are within the GEMM's accuracy).
  * For m <= 8 without a transform (decode batch sizes) the quantizer runs
  * inside the GEMM: its activation warp quantizes each K stage of x into the
  * MMA's shared-memory tile itself (the workspace's activation area is then

@@ -244,8 +244,6 @@ nvfp4::GemmParams gemm_params(const uint8_t *a_sf, int64_t m, const uint8_t *w_s
     g.err_flag = err;
     g.splits = 1;
     g.stages_per_split = (g.num_k64 + 3) / 4;
-    g.partials = nullptr;
-    g.part_ld = 0;
     g.group_offsets = nullptr;
     g.num_groups = 0;
     g.group_n = 0;
@@ -254,67 +252,55 @@ nvfp4::GemmParams gemm_params(const uint8_t *a_sf, int64_t m, const uint8_t *w_s
     return g;
 }
 
-// Split-K plan for small m (a single 128-row band), where the GEMM streams the
-// weight and one CTA per 128 x 256 output tile leaves SMs idle.  K is cut
-// into `splits` ranges of whole 256-element stages, choosing the count with
-// the least estimated cost in stage units: the stage-waves
-// ceil(tiles * splits / SMs) * ceil(stages / splits), plus, when split, the
-// fp32 partials each work item writes (m KB, stored row by row) and the reduce
-// reads back, priced at 4 * m KB-equivalents per item and wave against about
-// 36 KB of weight and scales per stage (measured: splitting pays for m = 1 on
-// every layer shape, but at m = 128 only when K is long).  Fewest splits on
-// ties; at most kMaxSplits and four waves of work items; every range
-// non-empty.  Returns the number of splits (1: none) and the stages per split.
+// Split-K plan for small m (a single 128-row band), where one CTA per 128 x 256
+// output tile leaves SMs idle while the weight streams.  K is cut into
+// `splits` ranges of whole 256-element stages; the ranges of a tile run as one
+// thread-block cluster and sum their partials through distributed shared
+// memory.  The count is the one with the fewest waves of clusters,
+// ceil(tiles / clusters resident at once), and among those the most ranges:
+// more SMs stream the weight, each a shorter range, while a second wave of
+// clusters costs more than any range length saves.  (Measured per layer for
+// every count at m = 1 .. 128 on the Llama and Qwen shapes: the largest
+// one-wave count was the fastest or within 1 us of it; e.g. Llama down at
+// m = 1, 16 tiles: 45.2 us unsplit, 16.9 us with 6 ranges, 26.7 us with 7,
+// whose clusters no longer fit in one wave.)  Every range non-empty; at most
+// kMaxSplits.  Returns the number of splits (1: none) and the stages per
+// split.
 int split_k_plan(const nvfp4::GemmParams &g, int num_sms, int *stages_per_split)
 {
     const int num_ks = (g.num_k64 + 3) / 4;
     *stages_per_split = num_ks;
     if (g.m > 128 || num_sms <= 0) return 1;
     const int64_t tiles = g.num_n_blk;
-    // costs in KB of traffic per SM (one stage ~ 36 KB)
     int best_s = 1;
-    int64_t best_cost = ((tiles + num_sms - 1) / num_sms) * num_ks * 36;
+    int64_t best_waves = (tiles + num_sms - 1) / num_sms;
     for (int s = 2; s <= nvfp4::kMaxSplits && s <= num_ks; ++s) {
         const int sps = (num_ks + s - 1) / s;
-        const int used = (num_ks + sps - 1) / sps;           // splits actually non-empty
-        const int64_t items = tiles * used;
-        if (items > 4 * (int64_t)num_sms) break;
-        const int64_t waves = (items + num_sms - 1) / num_sms;
-        const int64_t cost = waves * (sps * 36 + 4 * (int64_t)g.m);
-        if (cost < best_cost) {
-            best_cost = cost;
+        if ((num_ks + sps - 1) / sps != s) continue;         // some range would be empty
+        const int clusters = nvfp4::gemm_split_clusters(s, num_sms);
+        if (clusters < 1) continue;
+        const int64_t waves = (tiles + clusters - 1) / clusters;
+        if (waves <= best_waves) {
+            best_waves = waves;
             best_s = s;
         }
     }
-    if (best_s == 1) return 1;
-    const int sps = (num_ks + best_s - 1) / best_s;
-    *stages_per_split = sps;
-    return (num_ks + sps - 1) / sps;
+    *stages_per_split = (num_ks + best_s - 1) / best_s;
+    return best_s;
 }
 
-// Bytes of split-K partial sums for a split plan.
-size_t split_k_bytes(const nvfp4::GemmParams &g, int splits)
-{
-    return (size_t)splits * (size_t)g.m * (size_t)g.num_n_blk * 256 * sizeof(float);
-}
-
-// Room nvfp4_linear_workspace_bytes reserves for split-K partials, per row of
-// m: four waves of work items on a device of up to 160 SMs, 256 fp32 each.
-// A plan whose partials do not fit runs unsplit.
-constexpr size_t kSplitBytesPerRow = 4 * 160 * 256 * sizeof(float);
-
-// Launches the GEMM; with `partials` (scratch of partial_bytes bytes) and a
-// small m it may split K and finish with the reduce kernel.  after_quant: the
+// Launches the GEMM; with allow_split and a small m it may split K (the
+// linear entry points; nvfp4_gemm does not split).  after_quant: the
 // kernel just before on `s` is the quantizer of `a` (and nothing else), so the
 // GEMM may start as its programmatic dependent.
 // GEMM kernel choice: the CTA-pair kernel (256 x 256 tiles, half of B per SM)
 // for m > 128, the one-CTA kernel (which can split K) otherwise.  Both compute
 // the same result; nvfp4_gemm_ex lets a test pick either.
-enum GemmKernel { kGemmAuto = 0, kGemmOneCta = 1, kGemmPair = 2 };
+enum GemmKernel { kGemmAuto = 0, kGemmOneCta = 1, kGemmPair = 2, kGemmOneCtaSplit = 3 };
 
 nvfp4_status run_gemm(const uint8_t *a, const uint8_t *a_sf, int64_t m, const uint8_t *w, const uint8_t *w_sf,
                       int64_t n_w, int64_t n_out, int64_t k, const float *alpha, const void *bias, void *out,
-                      int64_t ldo, int num_sms, cudaStream_t s, float *partials = nullptr, size_t partial_bytes = 0,
+                      int64_t ldo, int num_sms, cudaStream_t s, bool allow_split = false,
                       bool after_quant = false, int kernel = kGemmAuto, uint64_t wait_ns = 0, int drill = 0,
                       bool mx = false, const nvfp4::QuantParams *fuse_quant = nullptr)
 {
@@ -324,14 +310,12 @@ nvfp4_status run_gemm(const uint8_t *a, const uint8_t *a_sf, int64_t m, const ui
     nvfp4::GemmParams g = gemm_params(a_sf, m, w_sf, n_w, n_out, k, alpha, bias, out, ldo, err, mx);
     if (wait_ns != 0) g.wait_ns = wait_ns;
     g.drill = drill;
-    if (partials != nullptr) {
+    if (allow_split && !(kernel == kGemmPair || (kernel == kGemmAuto && m > 128))) {
         int sps = 0;
         const int splits = split_k_plan(g, num_sms, &sps);
-        if (splits > 1 && split_k_bytes(g, splits) <= partial_bytes) {
+        if (splits > 1) {
             g.splits = splits;
             g.stages_per_split = sps;
-            g.partials = partials;
-            g.part_ld = (int64_t)g.num_n_blk * 256;
         }
     }
     const char *why = nullptr;
@@ -344,9 +328,7 @@ nvfp4_status run_gemm(const uint8_t *a, const uint8_t *a_sf, int64_t m, const ui
                  : nvfp4::launch_gemm(g, a, w, num_sms, s, &why, after_quant);
     }
     if (why) return fail(NVFP4_ERR_CUDA, "%s", why);
-    nvfp4_status st = launch_status(e, fuse_quant ? "fused linear kernel" : "GEMM kernel");
-    if (st != NVFP4_OK || g.splits == 1) return st;
-    return launch_status(nvfp4::launch_splitk_reduce(g, num_sms, s), "split-K reduce kernel");
+    return launch_status(e, fuse_quant ? "fused linear kernel" : "GEMM kernel");
 }
 
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
@@ -439,8 +421,7 @@ size_t nvfp4_linear_workspace_bytes(int64_t m, int64_t k, int64_t n_w)
 {
     (void)n_w;
     if (m <= 0 || k <= 0) return 0;
-    const size_t base = nvfp4::linear_min_workspace_bytes(m, k);
-    return m <= 128 ? base + align256(kSplitBytesPerRow * (size_t)m) : base;
+    return nvfp4::linear_min_workspace_bytes(m, k);
 }
 
 nvfp4_status nvfp4_quant_act(const void *x_bf16, int64_t m, int64_t k, int64_t ldx, const float *gs_dev,
@@ -551,8 +532,9 @@ nvfp4_status nvfp4_gemm_ex(const uint8_t *a_fp4, const uint8_t *a_sf, int64_t m,
                            const void *bias_bf16, void *out_bf16, int64_t ldo, int kernel, uint64_t wait_limit_ns,
                            int drill, nvfp4_stream_t stream)
 {
-    if (kernel < kGemmAuto || kernel > kGemmPair)
-        return fail(NVFP4_ERR_INVALID_ARG, "kernel must be 0 (automatic), 1 (one CTA) or 2 (CTA pair), got %d", kernel);
+    if (kernel < kGemmAuto || kernel > kGemmOneCtaSplit)
+        return fail(NVFP4_ERR_INVALID_ARG,
+                    "kernel must be 0 (automatic), 1 (one CTA), 2 (CTA pair) or 3 (one CTA, split K), got %d", kernel);
     if (kernel == kGemmPair && m > 0 && m <= 128)
         return fail(NVFP4_ERR_INVALID_ARG, "the CTA-pair kernel needs m > 128 (got %lld)", (long long)m);
     if (wait_limit_ns != 0 && (wait_limit_ns < 1000000ull || wait_limit_ns > 10000000000ull))
@@ -571,8 +553,11 @@ nvfp4_status nvfp4_gemm_ex(const uint8_t *a_fp4, const uint8_t *a_sf, int64_t m,
     if ((st = check_aliases(outs, 1, ins, 6)) != NVFP4_OK) return st;
     int num_sms = 0;
     if ((st = current_device(&num_sms)) != NVFP4_OK) return st;
+    // kernel 3: the one-CTA kernel with the linear's split-K plan (test hook)
+    const bool split = kernel == kGemmOneCtaSplit;
     return run_gemm(a_fp4, a_sf, m, w_fp4, w_sf, n_w, n_out, k, alpha_dev, bias_bf16, out_bf16, ldo, num_sms,
-                    reinterpret_cast<cudaStream_t>(stream), nullptr, 0, false, kernel, wait_limit_ns, drill);
+                    reinterpret_cast<cudaStream_t>(stream), split, false, split ? (int)kGemmOneCta : kernel,
+                    wait_limit_ns, drill);
 }
 
 nvfp4_status nvfp4_gemm(const uint8_t *a_fp4, const uint8_t *a_sf, int64_t m, const uint8_t *w_fp4,
@@ -613,24 +598,20 @@ nvfp4_status nvfp4_linear(const void *x_bf16, int64_t m, int64_t k, int64_t ldx,
     if ((st = current_device(&num_sms)) != NVFP4_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const nvfp4::QuantParams qp = quant_params(x_bf16, m, k, ldx, gs_dev, transform_bf16, bs, a_fp4, a_sf);
-    // the rest of the workspace (if any) takes split-K partial sums
-    float *partials = workspace_bytes > need ? reinterpret_cast<float *>(ws + need) : nullptr;
-    const size_t partial_bytes = workspace_bytes > need ? workspace_bytes - need : 0;
     if (m <= 8 && transform_bf16 == nullptr)        // decode sizes: the GEMM quantizes its own activation
         return run_gemm(a_fp4, a_sf, m, w_fp4, w_sf, n_w, n_out, k, alpha_dev, bias_bf16, out_bf16, ldo, num_sms,
-                        s, partials, partial_bytes, false, kGemmAuto, 0, 0, false, &qp);
+                        s, true, false, kGemmAuto, 0, 0, false, &qp);
     st = run_quant(qp, num_sms, s);
     if (st != NVFP4_OK) return st;
     return run_gemm(a_fp4, a_sf, m, w_fp4, w_sf, n_w, n_out, k, alpha_dev, bias_bf16, out_bf16, ldo, num_sms, s,
-                    partials, partial_bytes, true);
+                    true, true);
 }
 
 size_t nvfp4_mxfp4_linear_workspace_bytes(int64_t m, int64_t k, int64_t n_w)
 {
     (void)n_w;
     if (m <= 0 || k <= 0) return 0;
-    const size_t base = mx_min_workspace_bytes(m, k);
-    return m <= 128 ? base + align256(kSplitBytesPerRow * (size_t)m) : base;
+    return mx_min_workspace_bytes(m, k);
 }
 
 nvfp4_status nvfp4_mxfp4_gemm(const uint8_t *a_fp4, const uint8_t *a_sf, int64_t m, const uint8_t *w_fp4,
@@ -651,7 +632,7 @@ nvfp4_status nvfp4_mxfp4_gemm(const uint8_t *a_fp4, const uint8_t *a_sf, int64_t
     int num_sms = 0;
     if ((st = current_device(&num_sms)) != NVFP4_OK) return st;
     return run_gemm(a_fp4, a_sf, m, w_fp4, w_sf, n_w, n_out, k, nullptr, bias_bf16, out_bf16, ldo, num_sms,
-                    reinterpret_cast<cudaStream_t>(stream), nullptr, 0, false, kGemmAuto, 0, 0, true);
+                    reinterpret_cast<cudaStream_t>(stream), false, false, kGemmAuto, 0, 0, true);
 }
 
 nvfp4_status nvfp4_mxfp4_linear(const void *x_bf16, int64_t m, int64_t k, int64_t ldx, const uint8_t *w_fp4,
@@ -687,9 +668,8 @@ nvfp4_status nvfp4_mxfp4_linear(const void *x_bf16, int64_t m, int64_t k, int64_
     p.nbp = (p.nb + 3) / 4 * 4;
     st = launch_status(nvfp4::launch_quant_mx(p, num_sms, s), "MXFP4 quantize kernel");
     if (st != NVFP4_OK) return st;
-    float *partials = workspace_bytes > need ? reinterpret_cast<float *>(ws + need) : nullptr;
     return run_gemm(a_fp4, a_sf, m, w_fp4, w_sf, n_w, n_out, k, nullptr, bias_bf16, out_bf16, ldo, num_sms, s,
-                    partials, workspace_bytes > need ? workspace_bytes - need : 0, true, kGemmAuto, 0, 0, true);
+                    true, true, kGemmAuto, 0, 0, true);
 }
 
 nvfp4_status nvfp4_grouped_gemm(const uint8_t *a_fp4, const uint8_t *a_sf, int64_t rows,

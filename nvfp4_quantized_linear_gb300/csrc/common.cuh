@@ -41,7 +41,7 @@ struct QuantParams {
     uint16_t *y_out;         // nullptr, or [m, k] bf16: the transform result (row stride k)
 };
 
-constexpr int kMaxSplits = 16;       // split-K ranges at most
+constexpr int kMaxSplits = 8;        // split-K ranges at most (the portable cluster size)
 
 struct GemmParams {
     int32_t m, n_w, n_out, kp;
@@ -57,14 +57,13 @@ struct GemmParams {
     uint16_t *out;                   // bf16 bits
     int64_t ldo;
     unsigned int *err_flag;          // device error word
-    // Split-K (small m): K is cut into `splits` ranges of `stages_per_split`
-    // 256-element stages; each range writes raw fp32 sums (no alpha, bias or
-    // rounding) to partials[split][row][col] (row stride part_ld) and a reduce
-    // kernel finishes the epilogue.  splits == 1: the GEMM writes `out` itself.
+    // Split-K (small m, one-CTA kernel): K is cut into `splits` ranges of
+    // `stages_per_split` 256-element stages; the ranges of a tile run as the
+    // CTAs of one thread-block cluster, which sum their fp32 partials through
+    // distributed shared memory before the epilogue's alpha, bias and bf16
+    // rounding.  splits == 1: no split.
     int32_t splits;                  // 1 .. kMaxSplits
     int32_t stages_per_split;
-    float *partials;
-    int64_t part_ld;
     // Grouped GEMM (one-CTA kernel only): group_offsets [num_groups + 1] are
     // ascending row offsets, multiples of 128; the 128-row band of A at row r
     // belongs to the group g with offsets[g] <= r < offsets[g + 1] and is
@@ -96,18 +95,18 @@ cudaError_t launch_gemm(const GemmParams &p, const uint8_t *a, const uint8_t *w,
 // the bf16 activation; the GEMM's activation warp quantizes each stage of it
 // into shared memory itself, so no quantizer runs before it.  Launched as a
 // programmatic dependent of the kernel before it, whose completion both of its
-// producers wait for.  With splits > 1 the caller launches the split-K reduce.
+// producers wait for.
 cudaError_t launch_linear_fused(const GemmParams &p, const uint8_t *w, int num_sms, cudaStream_t s,
                                 const char **why);
-// Sum of the split-K partials, then alpha, bias and bf16 rounding into out;
-// launched as a programmatic dependent of the split GEMM just before it.
-cudaError_t launch_splitk_reduce(const GemmParams &p, int num_sms, cudaStream_t s);
+// Clusters of `splits` one-CTA GEMM blocks that can be resident at once (the
+// split-K plan's wave count).
+int gemm_split_clusters(int splits, int num_sms);
 // CTA-pair variant for m > 128 (tiles of 256 x 256 on two SMs).
 cudaError_t launch_gemm_pair(const GemmParams &p, const uint8_t *a, const uint8_t *w, int num_sms, cudaStream_t s,
                              const char **why, bool dependent = false);
 
-// Smallest workspace nvfp4_linear accepts: the quantized activation and its
-// scales (256-byte aligned inside); anything beyond it holds split-K partials.
+// Workspace of nvfp4_linear: the quantized activation and its scales (256-byte
+// aligned inside).
 size_t linear_min_workspace_bytes(int64_t m, int64_t k);
 
 // Records `msg` as this thread's last error (read by nvfp4_last_error_string)

@@ -25,7 +25,11 @@
 //               tcgen05.ld of finished accumulators, fma with alpha and bias, bf16 round into
 //               registers, release of the TMEM tile, then masked stores
 //               (rows < m, cols < n_out) that overlap the next tile's MMAs.
-//               With split-K the drain writes raw fp32 partial sums instead.
+// Split-K (small m): the K ranges of a tile run as the CTAs of one thread-block
+// cluster, one range each; the drain writes the raw fp32 sums into the CTA's
+// own shared memory, and after a cluster barrier every CTA sums its share of
+// the tile's columns over all ranks' partials (distributed shared memory, rank
+// order) and applies alpha, bias and the bf16 rounding.
 // Registers are moved between the warpgroups at start (setmaxnreg).
 // TMEM columns: [0,256) accumulator; stage s scales at 256 + 48 s (A: 16
 // columns = 4 K-steps x 4; B: 32 columns = 4 K-steps x 2 row-halves x 4).
@@ -113,46 +117,58 @@ __device__ __forceinline__ int group_of_band(const GemmParams &p, int mb)
 
 __device__ __forceinline__ Work work_of(int item, const GemmParams &p, int num_ks)
 {
-    const int per_split = p.num_m_blk * p.num_n_blk;
+    // split-K: consecutive items (the CTAs of one cluster) are the K ranges
+    // of one tile
     Work w;
-    w.split = item / per_split;
-    w.t = tile_coord(item - w.split * per_split, p.num_m_blk, p.num_n_blk);
+    w.split = item % p.splits;
+    w.t = tile_coord(item / p.splits, p.num_m_blk, p.num_n_blk);
     w.ks0 = w.split * p.stages_per_split;
     w.ks1 = min(num_ks, w.ks0 + p.stages_per_split);
     w.g = p.group_offsets != nullptr ? group_of_band(p, w.t.mb) : 0;
     return w;
 }
 
-// Sum of the split-K partials, then alpha, bias and bf16 rounding, for the
-// items (row, four columns) i = first, first + stride, ...: out[r, c] =
-// bf16(alpha * sum_s partials[s][r][c] + bias[c]), the splits added in index
-// order (deterministic), every split's load issued before the sum.
-__device__ __forceinline__ void reduce_partials(const GemmParams &p, int64_t first, int64_t stride)
+// Split-K partial sums in shared memory: row r of the tile at r * kPartLd
+// floats (256 columns, padded by 4 so that the 32 rows a warp writes at once
+// fall on different banks).
+constexpr int kPartLd = kBN + 4;
+static_assert((uint32_t)kBM * kPartLd * 4 <= kOffSfa, "the partials fit in the idle operand ring");
+
+// Cluster split-K finish, by the 256 epilogue threads of CTA `rank` of the
+// tile's p.splits CTAs: for the tile's 32-column chunks c with c % splits ==
+// rank, out[r, c] = bf16(alpha * (((part_0 + part_1) + part_2) + ...) + bias[c])
+// for rows r < m and columns < n_out, the ranks' partials read through
+// distributed shared memory and added in rank order (deterministic), all
+// loads of a group issued before the sum.
+__device__ __forceinline__ void cluster_reduce(const GemmParams &p, const Tile &t, uint32_t part_smem, uint32_t rank,
+                                               int tid)
 {
     const float alpha = p.alpha != nullptr ? __ldg(p.alpha) : 1.0f;
-    const int groups = (p.n_out + 3) / 4;
-    const int64_t total = (int64_t)p.m * groups;
-    const int64_t split_stride = (int64_t)p.m * p.part_ld;
-    for (int64_t i = first; i < total; i += stride) {
-        const int64_t r = i / groups;
-        const int c = (int)(i - r * groups) * 4;
-        const float *src = p.partials + r * p.part_ld + c;
-        float4 v[kMaxSplits];
+    const int rows = min(kBM, p.m - t.mb * kBM);
+    for (int c = (int)rank; c < kBN / 32; c += p.splits) {
+        for (int i = tid; i < rows * 8; i += kEpiWarps * 32) {
+            const int r = i >> 3;
+            const int col = c * 32 + (i & 7) * 4;                   // tile column
+            const int gcol = t.nb * kBN + col;
+            if (gcol >= p.n_out) continue;
+            const uint32_t off = part_smem + (uint32_t)(r * kPartLd + col) * 4;
+            float4 v[kMaxSplits];
 #pragma unroll
-        for (int sp = 0; sp < kMaxSplits; ++sp)
-            if (sp < p.splits) v[sp] = __ldcs(reinterpret_cast<const float4 *>(src + sp * split_stride));
-        float4 acc = v[0];
+            for (int sp = 0; sp < kMaxSplits; ++sp)
+                if (sp < p.splits) v[sp] = ld_dsmem_v4(mapa_shared_addr(off, (uint32_t)sp));
+            float4 acc = v[0];
 #pragma unroll
-        for (int sp = 1; sp < kMaxSplits; ++sp)
-            if (sp < p.splits) { acc.x += v[sp].x; acc.y += v[sp].y; acc.z += v[sp].z; acc.w += v[sp].w; }
-        const float a[4] = {acc.x, acc.y, acc.z, acc.w};
-        uint16_t *o = p.out + r * p.ldo + c;
+            for (int sp = 1; sp < kMaxSplits; ++sp)
+                if (sp < p.splits) { acc.x += v[sp].x; acc.y += v[sp].y; acc.z += v[sp].z; acc.w += v[sp].w; }
+            const float a[4] = {acc.x, acc.y, acc.z, acc.w};
+            uint16_t *o = p.out + (int64_t)(t.mb * kBM + r) * p.ldo + gcol;
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-            if (c + e < p.n_out) {
-                const float b = p.bias ? __uint_as_float((uint32_t)p.bias[c + e] << 16) : 0.0f;
-                o[e] = (uint16_t)bf16_bits_rn(__fmaf_rn(a[e], alpha, b));
-            }
+            for (int e = 0; e < 4; ++e)
+                if (gcol + e < p.n_out) {
+                    const float b = p.bias ? __uint_as_float((uint32_t)p.bias[gcol + e] << 16) : 0.0f;
+                    o[e] = (uint16_t)bf16_bits_rn(__fmaf_rn(a[e], alpha, b));
+                }
+        }
     }
 }
 
@@ -181,7 +197,14 @@ __device__ __forceinline__ void fused_act_producer(const GemmParams &p, const CU
     griddep_wait();                                  // x and gs may be the preceding kernel's output
     const QuantParams &q = p.quant;
     const float gs = __ldg(q.gs);
-    const float *inv_tab = reinterpret_cast<const float *>(smem + kOffInvTab);
+    // gs / e4m3(code) for the 128 scale codes, built by this warp from the gs
+    // read after the wait (the preceding kernel may have written gs)
+    float *inv_tab = reinterpret_cast<float *>(smem + kOffInvTab);
+    for (int c = lane; c < 128; c += 32) {
+        const float d = e4m3_to_f32((uint32_t)c);
+        inv_tab[c] = (d == 0.0f) ? 0.0f : __fdiv_rn(gs, d);
+    }
+    __syncwarp();
     const uint64_t pol = l2_policy_evict_last();     // every column tile's CTAs read the same slices
     int stage = 0;
     uint32_t phase = 0;
@@ -285,7 +308,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
-    if constexpr (kFused) quant_core::fill_inv_table(reinterpret_cast<float *>(smem + kOffInvTab), __ldg(p.quant.gs));
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -295,7 +317,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int num_ks = (p.num_k64 + 3) / 4;
     const int n_bands_w = (p.n_w + 127) / 128;
 
-    if (threadIdx.x == 0) griddep_launch_dependents();   // the split-K reduce may get resident
+    // The next kernel on the stream, if launched as a programmatic dependent
+    // (this library's quantizer or GEMM), may get resident now: it waits for
+    // this grid before it reads anything.
+    if (threadIdx.x == 0) griddep_launch_dependents();
 
     // Roles by warpgroup; each warpgroup first resizes its register file.
     if (warp >= kEpiWarp0) {
@@ -332,8 +357,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t r0[32], r1[32];
 
             if (p.splits > 1) {
-                // split-K: raw fp32 sums of this K range for rows < m
-                float *dst = p.partials + ((int64_t)wk.split * p.m + row) * p.part_ld + col_base;
+                // split-K: raw fp32 sums of this K range for rows < m, into this
+                // CTA's shared memory (the operand ring: every stage of the
+                // CTA's one work item has been consumed)
+                const uint32_t dst = smem_u32(smem) + (uint32_t)((row - t.mb * kBM) * kPartLd + hcol) * 4;
                 if (n_cols > 0) tmem_ld_32cols(acc, r0);
 #pragma unroll
                 for (int ch = 0; ch < kEpiCols / 32; ++ch) {
@@ -346,8 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (row < p.m) {
 #pragma unroll
                             for (int v = 0; v < 8; ++v)
-                                *reinterpret_cast<uint4 *>(dst + ch * 32 + 4 * v) =
-                                    make_uint4(cur[4 * v], cur[4 * v + 1], cur[4 * v + 2], cur[4 * v + 3]);
+                                st_shared_v4(dst + (uint32_t)(ch * 32 + 4 * v) * 4, cur[4 * v], cur[4 * v + 1],
+                                             cur[4 * v + 2], cur[4 * v + 3]);
                         }
                     }
                 }
@@ -411,6 +438,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (lane == 0) bulk_wait_group<0>();                    // all output written before the CTA exits
+        if (p.splits > 1) {
+            // Cluster split-K: the first barrier phase completes once every
+            // rank's partials are in its shared memory (this warp's arrival
+            // releases its own); then this CTA sums its share of the columns.
+            // The second phase, whose wait follows below, keeps the partials
+            // until every peer has read them.
+            cluster_arrive_release();
+            cluster_wait_acquire();
+            cluster_reduce(p, work_of(blockIdx.x, p, num_ks).t, smem_u32(smem), cluster_ctarank(),
+                           (int)threadIdx.x - kEpiWarp0 * 32);
+            cluster_arrive_release();
+        }
     } else if (warp >= kSfWarp0) {
         setmaxnreg_dec<kRegsSf>();
         // ----------------------------------------------- scale staging --
@@ -527,7 +566,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (warp == 2 && p.splits == 1 && p.bias != nullptr) {
             // ---------------------------------------------------- bias loader --
             // The bias of each tile into one of two shared buffers, for the
-            // four epilogue warps (bias_full / bias_empty per buffer).
+            // four epilogue warps (bias_full / bias_empty per buffer).  As a
+            // programmatic dependent this grid may start before the kernel
+            // that writes the bias has finished: wait for it first.
+            griddep_wait();
             uint16_t *s_bias_all = reinterpret_cast<uint16_t *>(smem + kOffBias);
             int it = 0;
             for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
@@ -602,41 +644,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
+    if (p.splits > 1 && warp < kEpiWarp0) {
+        // the other warps' arrivals on both phases of the epilogue's cluster
+        // barrier (they hold nothing the reduction reads)
+        cluster_arrive_release();
+        cluster_wait_acquire();
+        cluster_arrive_release();
+    }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
+    if (p.splits > 1) cluster_wait_acquire();          // every peer has read this CTA's partials
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Split-K finish: out[r, c] = bf16(alpha * sum_s partials[s][r][c] + bias[c])
-// for r < m, c < n_out, the splits summed in index order (deterministic).
-// Each thread handles four consecutive columns.
-__global__ void __launch_bounds__(256) splitk_reduce_kernel(const GemmParams p)
-{
-    griddep_wait();                                 // the split GEMM's partials are complete
-    reduce_partials(p, (int64_t)blockIdx.x * blockDim.x + threadIdx.x, (int64_t)gridDim.x * blockDim.x);
-}
-
 }  // namespace
-
-cudaError_t launch_splitk_reduce(const GemmParams &p, int num_sms, cudaStream_t s)
-{
-    const int64_t total = (int64_t)p.m * ((p.n_out + 3) / 4);
-    int64_t blocks = (total + 255) / 256;
-    if (blocks > (int64_t)num_sms * 8) blocks = (int64_t)num_sms * 8;
-    if (blocks < 1) blocks = 1;
-    if (p.splits < 2 || p.splits > kMaxSplits) return cudaErrorInvalidValue;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr.val.programmaticStreamSerializationAllowed = 1;
-    cfg.gridDim = dim3((unsigned)blocks, 1, 1);
-    cfg.blockDim = dim3(256, 1, 1);
-    cfg.stream = s;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, p);
-}
 
 namespace {
 
@@ -675,20 +697,37 @@ cudaError_t launch_one_cta(const GemmParams &p, const uint8_t *a, const uint8_t 
             return cudaErrorInvalidValue;
         }
     } else {
-        tmOut = tmA;                                    // not used: split-K writes partial sums
+        tmOut = tmA;                                    // not used: the cluster reduction stores the output
     }
-    const int tiles = p.num_m_blk * p.num_n_blk * p.splits;
-    const int grid = tiles < num_sms ? tiles : num_sms;
+    // Persistent over the tiles (one CTA per SM at most); with split-K one CTA
+    // per (tile, K range), the ranges of a tile forming one cluster.
+    const int items = p.num_m_blk * p.num_n_blk * p.splits;
+    if (p.splits > 1 && (p.splits > kMaxSplits || p.num_m_blk != 1 || p.group_offsets != nullptr)) {
+        *why = "split-K takes one 128-row band, no groups, at most 8 ranges";
+        return cudaErrorInvalidValue;
+    }
+    const int grid = p.splits > 1 ? items : (items < num_sms ? items : num_sms);
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attrs[2];
+    int n_attrs = 0;
+    if (dependent) {
+        attrs[n_attrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[n_attrs].val.programmaticStreamSerializationAllowed = 1;
+        ++n_attrs;
+    }
+    if (p.splits > 1) {
+        attrs[n_attrs].id = cudaLaunchAttributeClusterDimension;
+        attrs[n_attrs].val.clusterDim.x = (unsigned)p.splits;
+        attrs[n_attrs].val.clusterDim.y = 1;
+        attrs[n_attrs].val.clusterDim.z = 1;
+        ++n_attrs;
+    }
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = s;
-    cfg.attrs = dependent ? &attr : nullptr;
-    cfg.numAttrs = dependent ? 1 : 0;
+    cfg.attrs = n_attrs ? attrs : nullptr;
+    cfg.numAttrs = n_attrs;
     CUtensorMap tmX = tmA;                              // the plain GEMM reads no bf16 activation
     if (fused && !make_x_slice_map(&tmX, p.quant.x, (uint64_t)p.quant.k, (uint64_t)p.quant.m, (uint64_t)p.quant.ldx)) {
         *why = "cuTensorMapEncodeTiled failed for the activation";
@@ -700,6 +739,46 @@ cudaError_t launch_one_cta(const GemmParams &p, const uint8_t *a, const uint8_t 
 }
 
 }  // namespace
+
+int gemm_split_clusters(int splits, int num_sms)
+{
+    // clusters of `splits` one-CTA GEMM blocks resident at once on this device
+    // (queried once per device and size; the SMs / splits if the query fails)
+    static int cached_dev = -1;
+    static int cached[kMaxSplits + 1];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (splits < 2 || splits > kMaxSplits) return num_sms;
+    if (cached_dev != dev) {
+        for (int i = 0; i <= kMaxSplits; ++i) cached[i] = 0;
+        cached_dev = dev;
+    }
+    if (cached[splits] == 0) {
+        int clusters = 0;
+        cudaError_t e = cudaFuncSetAttribute(gemm_nvf4_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemBytes);
+        if (e == cudaSuccess) {
+            cudaLaunchConfig_t probe = {};
+            cudaLaunchAttribute attr;
+            attr.id = cudaLaunchAttributeClusterDimension;
+            attr.val.clusterDim.x = (unsigned)splits;
+            attr.val.clusterDim.y = 1;
+            attr.val.clusterDim.z = 1;
+            probe.gridDim = dim3((unsigned)(splits * (num_sms / splits)), 1, 1);
+            probe.blockDim = dim3(kThreads, 1, 1);
+            probe.dynamicSmemBytes = kSmemBytes;
+            probe.attrs = &attr;
+            probe.numAttrs = 1;
+            e = cudaOccupancyMaxActiveClusters(&clusters, gemm_nvf4_kernel<false, false>, &probe);
+        }
+        if (e != cudaSuccess || clusters < 1) {
+            cudaGetLastError();
+            clusters = num_sms / splits;
+        }
+        cached[splits] = clusters;
+    }
+    return cached[splits];
+}
 
 cudaError_t launch_gemm(const GemmParams &p, const uint8_t *a, const uint8_t *w, int num_sms, cudaStream_t s,
                         const char **why, bool dependent)

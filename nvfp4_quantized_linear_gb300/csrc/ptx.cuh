@@ -464,6 +464,26 @@ __device__ __forceinline__ uint32_t mapa_shared(const void *local, uint32_t rank
     return r;
 }
 
+// The same for a shared::cta address given as a 32-bit value.
+__device__ __forceinline__ uint32_t mapa_shared_addr(uint32_t local, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+
+// 16-byte load from the shared memory of a CTA of this cluster (shared::cluster
+// address from mapa).
+__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t cluster_addr)
+{
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(cluster_addr)
+                 : "memory");
+    return v;
+}
+
 // Arrive on an mbarrier of a CTA of this cluster (shared::cluster address from
 // mapa) with the instruction's default semantics (release, CTA scope): the
 // arrival is performed at the barrier's CTA.  Much cheaper than a
@@ -506,6 +526,19 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity
             return false;
         }
     }
+}
+
+// Split cluster barrier (any thread, not necessarily warp-converged): every
+// thread of the cluster arrives once per phase, and a thread's wait returns
+// once all have arrived; release / acquire at cluster scope.
+__device__ __forceinline__ void cluster_arrive_release()
+{
+    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait_acquire()
+{
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
 }
 
 __device__ __forceinline__ void cluster_sync_all()

@@ -89,10 +89,12 @@ def test_size_queries(lib):
     ws = nv.nvfp4_linear_workspace_bytes(100, 1000, 512)
     assert ws >= nv.nvfp4_packed_bytes(100, 1000) + nv.nvfp4_scale_bytes(100, 1000)
     assert nv.nvfp4_linear_workspace_bytes(0, 1000, 512) == 0
-    # m <= 128 adds room for split-K partials (640 x 256 fp32 per row); larger m does not
+    # the quantized activation and its scales, each 256-byte aligned (split-K
+    # partial sums stay in the CTAs' shared memory, at every m)
     base = lambda m, k: (nv.nvfp4_packed_bytes(m, k) + 255) // 256 * 256 + (nv.nvfp4_scale_bytes(m, k) + 255) // 256 * 256
-    assert ws == base(100, 1000) + 640 * 256 * 4 * 100
+    assert ws == base(100, 1000)
     assert nv.nvfp4_linear_workspace_bytes(129, 1000, 512) == base(129, 1000)
+    assert nv.nvfp4_linear_workspace_bytes(1, 14336, 4096) == base(1, 14336)
 
 
 def quant(lib, x=A, m=16, k=256, ldx=256, gs=B, t=None, bs=0, out=C, sf=D):

@@ -22,7 +22,7 @@ def _weights(n, k, seed):
 
 
 @pytest.mark.parametrize("m,k,n,bs,dynamic", [
-    (16, 1024, 768, 0, False),       # one-CTA GEMM with split-K and its reduce kernel
+    (16, 1024, 768, 0, False),       # one-CTA GEMM with split-K in a cluster
     (256, 512, 512, 0, False),       # CTA-pair GEMM
     (256, 512, 512, 16, False),      # transform quantizer in the graph
     (64, 1024, 512, 0, True),        # dynamic global scale (memset + amax + finalize) in the graph

@@ -110,38 +110,48 @@ def test_linear_rejects_small_workspace():
 
 SPLIT_K = [syn.Problem("splitk", f"m{m}-n{n}-k{k}", m, k, n, seed=1300 + i, bias=bias, n_out=n_out)
            for i, (m, k, n, n_out, bias) in enumerate([
-               (1, 4096, 256, None, False),      # one output tile: 16 splits of one stage
+               (1, 4096, 256, None, False),      # one output tile: a cluster of 8 ranges of 2 stages
                (5, 4104, 1024, 1000, True),      # ragged K (65 k-steps), sliced output, bias
                (64, 14336, 4096, None, True),    # Llama down_proj width at decode size
-               (128, 14336, 512, 500, False),    # full band, 2 tiles, long K: 14 splits of 4 stages
+               (128, 14336, 512, 500, False),    # full band, 2 tiles, long K: 7 stages per range
                (33, 64, 256, None, True),        # a single K stage: no split
            ])]
 
 
 @pytest.mark.parametrize("p", SPLIT_K, ids=_ids(SPLIT_K))
 def test_split_k_matches_oracle_and_unsplit(p):
-    """Small m with the full workspace takes the split-K path (fp32 partials +
-    ordered reduce); it must match the oracle on every element, agree with the
-    unsplit GEMM (minimum workspace) to fp32-summation-order accuracy, and be
-    bit-identical across calls."""
+    """Small m: nvfp4_linear splits K across the CTAs of a cluster (fp32
+    partials summed in shared memory, rank order).  It must match the oracle on
+    every element, agree with the unsplit one-CTA GEMM on the same quantized
+    operands to fp32-summation-order accuracy, equal the split GEMM test hook
+    (nvfp4_gemm_ex kernel 3) bit for bit, and be bit-identical across calls."""
     L = syn.make_layer(p, device="cuda")
     m, k, n_out = p.m, p.k, p.n_keep
     w_fp4, w_sf = nv.prepare_weight(L.w, dev_scalar(L.gs_w))
     gs, alpha = dev_scalar(L.gs_x), dev_scalar(L.alpha)
-    full = nv.nvfp4_linear_workspace_bytes(m, k, p.n)
-    small = (nv.nvfp4_packed_bytes(m, k) + 255) // 256 * 256 + (nv.nvfp4_scale_bytes(m, k) + 255) // 256 * 256
-    assert full > small
+    ws_bytes = nv.nvfp4_linear_workspace_bytes(m, k, p.n)
+    ldo = (n_out + 7) // 8 * 8                           # output rows 16-byte aligned
+
+    def fresh():
+        return torch.full((m, ldo), float("nan"), dtype=torch.bfloat16, device="cuda")[:, :n_out]
+
     outs = []
-    for ws_bytes in (full, full, small):
+    for _ in range(2):
         ws = torch.full((ws_bytes,), 0xA5, dtype=torch.uint8, device="cuda")
-        ldo = (n_out + 7) // 8 * 8                       # output rows 16-byte aligned
-        out = torch.full((m, ldo), float("nan"), dtype=torch.bfloat16, device="cuda")[:, :n_out]
+        out = fresh()
         nv.nvfp4_linear(L.x, m, k, L.x.stride(0), gs, None, 0, w_fp4, w_sf, p.n, n_out, alpha, L.bias,
                         out, out.stride(0), ws, ws_bytes)
-        torch.cuda.synchronize()
-        nv.nvfp4_device_error()
         outs.append(out)
+    a_fp4, a_sf = nv.quant_act(L.x, gs)
+    for kernel in (1, 3):                                # unsplit, split with the linear's plan
+        out = fresh()
+        nv.nvfp4_gemm_ex(a_fp4, a_sf, m, w_fp4, w_sf, p.n, n_out, k, alpha, L.bias, out, out.stride(0),
+                         kernel=kernel)
+        outs.append(out)
+    torch.cuda.synchronize()
+    nv.nvfp4_device_error()
     assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16)), "split-K not deterministic"
+    assert torch.equal(outs[0].view(torch.int16), outs[3].view(torch.int16)), "linear differs from the split GEMM"
     a, sa = oracle.quantize(syn.bf16_bits(L.x), L.gs_x, k=k)
     b, sb = oracle.quantize(syn.bf16_bits(L.w[:n_out]), L.gs_w, k=k)
     bias = syn.bf16_bits(L.bias[:n_out]) if L.bias is not None else None

@@ -101,22 +101,21 @@ def test_mxfp4_gemm_exact_power_of_two_case_is_bit_exact():
 
 @pytest.mark.parametrize("m,k,n", [(1, 14336, 4096), (64, 4096, 2048)])
 def test_mxfp4_linear_split_k_matches_unsplit(m, k, n):
-    """Small m with the full workspace splits K (fp32 partials + ordered
-    reduce); against the oracle and the unsplit GEMM (minimum workspace)."""
+    """Small m: the MXFP4 linear splits K across the CTAs of a cluster (fp32
+    partials summed in shared memory); against the oracle and the unsplit
+    MXFP4 GEMM on the same quantized operands."""
     x = syn.bf16_normal((m, k), 1.0, 6200 + m, device="cuda")
     w = syn.bf16_normal((n, k), 0.02, 6201, device="cuda")
     w_fp4, w_sf = _quant(w)
-    full = nv.nvfp4_mxfp4_linear_workspace_bytes(m, k, n)
-    small = (nv.nvfp4_packed_bytes(m, k) + 255) // 256 * 256 + (nv.nvfp4_mxfp4_scale_bytes(m, k) + 255) // 256 * 256
-    assert full > small
-    outs = []
-    for ws_bytes in (full, small):
-        ws = torch.full((ws_bytes,), 0xA5, dtype=torch.uint8, device="cuda")
-        outs.append(nv.mxfp4_linear(x, w_fp4, w_sf, k, n, workspace=ws))
+    ws = torch.full((nv.nvfp4_mxfp4_linear_workspace_bytes(m, k, n),), 0xA5, dtype=torch.uint8, device="cuda")
+    lin = nv.mxfp4_linear(x, w_fp4, w_sf, k, n, workspace=ws)
+    a_fp4, a_sf = _quant(x)
+    unsplit = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+    nv.nvfp4_mxfp4_gemm(a_fp4, a_sf, m, w_fp4, w_sf, n, n, k, None, unsplit, n)
     torch.cuda.synchronize()
     nv.nvfp4_device_error()
     rows = np.arange(m)
     cols = sample_indices(n, 384, 6202, must=tile_edges(n, 128))
     ref = _oracle(x, w, None, k, rows, cols)
-    for o in outs:
-        assert_gemm_close(bf16_to_f64(o)[rows][:, cols], ref, "mxfp4 linear split/unsplit")
+    for o, what in ((lin, "split"), (unsplit, "unsplit")):
+        assert_gemm_close(bf16_to_f64(o)[rows][:, cols], ref, f"mxfp4 linear {what}")

@@ -58,7 +58,7 @@ def test_gemm_ex_rejects_bad_choices():
     sf = torch.zeros(nv.nvfp4_scale_bytes(64, 64), dtype=torch.uint8, device="cuda")
     out = torch.empty((64, 64), dtype=torch.bfloat16, device="cuda")
     one = dev_scalar(1.0)
-    for kw in (dict(kernel=3), dict(kernel=2), dict(wait_limit_ns=5), dict(drill=2)):
+    for kw in (dict(kernel=4), dict(kernel=-1), dict(kernel=2), dict(wait_limit_ns=5), dict(drill=2)):
         with pytest.raises(nv.Nvfp4Error) as e:
             nv.nvfp4_gemm_ex(x, sf, 64, x, sf, 64, 64, 64, one, None, out, 64, **kw)
         assert e.value.status == 1, kw
