@@ -82,9 +82,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
-    ap.add_argument("--case", choices=["quant", "gemm", "linear"],
+    ap.add_argument("--case", choices=["quant", "gemm", "linear", "step"],
                     help="run one kernel on synthetic data a few times and exit (for ncu captures): "
-                         "--m/--k/--n/--bs choose the shape, --steps the launches")
+                         "--m/--k/--n/--bs choose the shape, --steps the launches; 'step': the --workload's "
+                         "layers at --m through nvfp4_linear, --steps times")
     ap.add_argument("--k", type=int, default=4096)
     ap.add_argument("--n", type=int, default=4096)
     ap.add_argument("--bs", type=int, default=0, help="--case: transform block size (0 = none)")
@@ -94,7 +95,7 @@ def parse_args(argv=None):
     a = ap.parse_args(argv)
     a.warmup = max(a.warmup, 3)
     if a.m is None:
-        a.m = WORKLOADS[a.workload][1] if not a.case else 8192
+        a.m = WORKLOADS[a.workload][1] if a.case in (None, "step") else 8192
     return a
 
 
@@ -873,13 +874,26 @@ def run_reference(args, rank, world):
 def run_case(args):
     """One kernel on a synthetic N(0, 1) activation [M, K] (transformed by a
     random bs x bs Hadamard block when --bs > 0) and an N(0, 0.02) weight
-    [N, K], launched --steps times; prints 'ok'."""
+    [N, K], launched --steps times; or ('step') the workload's layers at --m
+    through nvfp4_linear, --steps times.  Prints 'ok'."""
     import torch
 
     import nvfp4_quantized_linear_gb300 as nv
     from nvfp4_quantized_linear_gb300 import synthetic as syn
     nv.build()
     dev = torch.device("cuda", 0)
+    if args.case == "step":
+        layers = setup_layers(layer_problems(args.workload, args.m, 0), dev)
+        stream = torch.cuda.current_stream().cuda_stream
+        for _ in range(args.steps):
+            for l in layers:
+                p = l["p"]
+                nv.nvfp4_linear(l["x"], p.m, p.k, p.k, l["gs_x"], None, 0, l["w_fp4"], l["w_sf"], p.n, p.n,
+                                l["alpha"], None, l["out"], p.n, l["ws"], l["ws"].numel(), stream)
+        torch.cuda.synchronize()
+        nv.nvfp4_device_error()
+        print("ok")
+        return
     m, k, n, bs = args.m, args.k, args.n, args.bs
     x = syn.bf16_normal((m, k), 1.0, 3, device=dev)
     t = syn.random_hadamard_transform(bs, seed=bs).to(dev) if bs else None

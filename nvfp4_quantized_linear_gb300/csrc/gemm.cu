@@ -183,16 +183,17 @@ __device__ __forceinline__ void cluster_reduce(const GemmParams &p, const Tile &
 // block scales into the stage's four scale tiles, zeroed first so that rows
 // >= m contribute nothing (their A bytes are finite FP4 codes whatever they
 // hold).  Then the async-proxy fence and the stage's second `full` arrival.
-// The slice's copy is requested when the stage frees, together with the
-// stage's weights, so it adds no latency of its own.
+// The slice's copy is requested by the weight producer together with the
+// stage's weights, as soon as the stage frees (up to kStages ahead): a warp
+// that fetched each slice itself after quantizing the previous one paid the
+// copy's round trip once per stage.
 constexpr uint32_t kXSliceOff = 16 * 128;                    // rows 16.. of an A tile
 constexpr uint32_t kXSliceBytes = kXSliceRows * 256 * 2;     // 16 rows x 256 bf16
 static_assert(kXSliceOff + kXSliceBytes <= kABytes, "the activation slice fits in the A tile's spare rows");
 
 template <bool kFused>
-__device__ __forceinline__ void fused_act_producer(const GemmParams &p, const CUtensorMap *tmX, uint8_t *smem,
-                                                   uint64_t *full, uint64_t *empty, uint64_t *x_full, int num_ks,
-                                                   int lane)
+__device__ __forceinline__ void fused_act_producer(const GemmParams &p, uint8_t *smem, uint64_t *full,
+                                                   uint64_t *x_full, int num_ks, int lane)
 {
     griddep_wait();                                  // x and gs may be the preceding kernel's output
     const QuantParams &q = p.quant;
@@ -205,24 +206,20 @@ __device__ __forceinline__ void fused_act_producer(const GemmParams &p, const CU
         inv_tab[c] = (d == 0.0f) ? 0.0f : __fdiv_rn(gs, d);
     }
     __syncwarp();
-    const uint64_t pol = l2_policy_evict_last();     // every column tile's CTAs read the same slices
     int stage = 0;
     uint32_t phase = 0;
     for (int tile = blockIdx.x; tile < p.num_m_blk * p.num_n_blk * p.splits; tile += gridDim.x) {
         const Work wk = work_of(tile, p, num_ks);
         for (int ks = wk.ks0; ks < wk.ks1; ++ks) {
-            if (!__all_sync(~0u, mbar_wait(&empty[stage], phase ^ 1, p.err_flag, kErrTimeout, p.wait_ns))) return;
+            // the slice landed (it was requested after the stage freed, so the
+            // stage's A and scale tiles may be rewritten too)
+            if (!__all_sync(~0u, mbar_wait(&x_full[stage], phase, p.err_flag, kErrTimeout, p.wait_ns))) return;
             uint8_t *a_tile = smem + kOffA + stage * kABytes;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&x_full[stage], kXSliceBytes);
-                tma_load_2d(a_tile + kXSliceOff, tmX, &x_full[stage], ks * 256, 0, pol);
-            }
             const uint32_t a_dst = smem_u32(a_tile);
             const uint32_t x_src = a_dst + kXSliceOff;
             const uint32_t sf_dst = smem_u32(smem + kOffSfa + stage * kSfaBytes);
 #pragma unroll
             for (int i = 0; i < (int)kSfaBytes / 16 / 32; ++i) st_shared_v4(sf_dst + (lane + 32 * i) * 16, 0, 0, 0, 0);
-            if (!__all_sync(~0u, mbar_wait(&x_full[stage], phase, p.err_flag, kErrTimeout, p.wait_ns))) return;
             for (int b = lane; b < q.m * 16; b += 32) {
                 const int r = b >> 4, j = b & 15;
                 quant_core::Raw16 raw;
@@ -507,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         setmaxnreg_dec<kRegsCtl>();
         if (kFused && warp == 0) {
-            if (!p.drill) fused_act_producer<kFused>(p, &tmX, smem, full, empty, x_full, num_ks, lane);
+            if (!p.drill) fused_act_producer<kFused>(p, smem, full, x_full, num_ks, lane);
         } else if ((warp == 0 || warp == 3) && lane == 0 && !p.drill) {   // (a timeout drill issues no copies)
             // ----------------------------------------------------- producers --
             // Two threads fill the ring, each with its half of every stage:
@@ -546,6 +543,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         bulk_load(smem + kOffSfa + stage * kSfaBytes,
                                   p.sfa + t.mb * p.sfa_band_bytes + (int64_t)ks * kT * 512, sf_bytes, &full[stage], pol);
                     } else {
+                        if constexpr (kFused) {
+                            // the stage's activation slice for the fused linear's activation warp
+                            // (every column tile's CTAs read the same slices: keep them in L2)
+                            mbar_arrive_expect_tx(&x_full[stage], kXSliceBytes);
+                            tma_load_2d(smem + kOffA + stage * kABytes + kXSliceOff, &tmX, &x_full[stage], ks * 256, 0,
+                                        l2_policy_evict_last());
+                        }
                         mbar_arrive_expect_tx(&full[stage], kBBytes + sf_bytes * halves);
                         tma_load_2d(smem + kOffB + stage * kBBytes, &tmB, &full[stage], ks * kBKBytes, b_row0, pol);
                         for (int h = 0; h < halves; ++h)    // halves == 2 implies band t.nb*2+1 exists
@@ -561,8 +565,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             (void)n_bands_w;
             // Every copy this thread issued has landed before the CTA may exit.
             for (int s = 0; s < kStages; ++s)
-                if (issued_mask & (1u << s))
+                if (issued_mask & (1u << s)) {
+                    if (kFused && !act_side)
+                        mbar_wait(&x_full[s], (issued_phase >> s) & 1u, p.err_flag, kErrTimeout, p.wait_ns);
                     mbar_wait(&full[s], (issued_phase >> s) & 1u, p.err_flag, kErrTimeout, p.wait_ns);
+                }
         } else if (warp == 2 && p.splits == 1 && p.bias != nullptr) {
             // ---------------------------------------------------- bias loader --
             // The bias of each tile into one of two shared buffers, for the
