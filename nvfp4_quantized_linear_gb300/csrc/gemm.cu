@@ -132,42 +132,67 @@ __device__ __forceinline__ Work work_of(int item, const GemmParams &p, int num_k
 // floats (256 columns, padded by 4 so that the 32 rows a warp writes at once
 // fall on different banks).
 constexpr int kPartLd = kBN + 4;
+// Up to this many rows below m in an epilogue warp's 32, the rows are written
+// straight from registers instead of through the staging buffer and the TMA.
+constexpr int kDirectStoreRows = 16;
 static_assert((uint32_t)kBM * kPartLd * 4 <= kOffSfa, "the partials fit in the idle operand ring");
 
 // Cluster split-K finish, by the 256 epilogue threads of CTA `rank` of the
-// tile's p.splits CTAs: for the tile's 32-column chunks c with c % splits ==
-// rank, out[r, c] = bf16(alpha * (((part_0 + part_1) + part_2) + ...) + bias[c])
-// for rows r < m and columns < n_out, the ranks' partials read through
-// distributed shared memory and added in rank order (deterministic), all
-// loads of a group issued before the sum.
+// tile's p.splits CTAs.  The tile's valid 4-column groups (rows r < m,
+// columns < n_out, row-major) are cut into p.splits equal ranges; for each
+// group of its range this CTA forms out[r, c..c+3] = bf16(alpha * (((part_0 +
+// part_1) + part_2) + ...) + bias[c]), the ranks' partials added in rank order
+// (deterministic), its own from its shared memory and the others' through
+// distributed shared memory, all loads of a group issued before the sum.
+// Equal ranges rather than whole column chunks per rank: at m = 128 the
+// distributed-shared-memory reads (m x 1 KB per rank) set the reduction's
+// time, and chunks of 32 columns gave two ranks of six twice the reads.
 __device__ __forceinline__ void cluster_reduce(const GemmParams &p, const Tile &t, uint32_t part_smem, uint32_t rank,
                                                int tid)
 {
     const float alpha = p.alpha != nullptr ? __ldg(p.alpha) : 1.0f;
     const int rows = min(kBM, p.m - t.mb * kBM);
-    for (int c = (int)rank; c < kBN / 32; c += p.splits) {
-        for (int i = tid; i < rows * 8; i += kEpiWarps * 32) {
-            const int r = i >> 3;
-            const int col = c * 32 + (i & 7) * 4;                   // tile column
-            const int gcol = t.nb * kBN + col;
-            if (gcol >= p.n_out) continue;
-            const uint32_t off = part_smem + (uint32_t)(r * kPartLd + col) * 4;
-            float4 v[kMaxSplits];
+    const int cols = min(kBN, p.n_out - t.nb * kBN);
+    const int quads = (cols + 3) >> 2;
+    const int items = rows * quads;
+    const int i0 = (int)((int64_t)items * rank / p.splits);
+    const int i1 = (int)((int64_t)items * (rank + 1) / p.splits);
+    for (int i = i0 + tid; i < i1; i += kEpiWarps * 32) {
+        const int r = i / quads;
+        const int col = (i - r * quads) * 4;                        // tile column
+        const int gcol = t.nb * kBN + col;
+        const uint32_t off = part_smem + (uint32_t)(r * kPartLd + col) * 4;
+        float4 v[kMaxSplits];
 #pragma unroll
-            for (int sp = 0; sp < kMaxSplits; ++sp)
-                if (sp < p.splits) v[sp] = ld_dsmem_v4(mapa_shared_addr(off, (uint32_t)sp));
-            float4 acc = v[0];
+        for (int sp = 0; sp < kMaxSplits; ++sp)
+            if (sp < p.splits) {
+                if (sp == (int)rank) {
+                    const uint4 u = ld_shared_v4(off);
+                    v[sp] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
+                                        __uint_as_float(u.w));
+                } else {
+                    v[sp] = ld_dsmem_v4(mapa_shared_addr(off, (uint32_t)sp));
+                }
+            }
+        float4 acc = v[0];
 #pragma unroll
-            for (int sp = 1; sp < kMaxSplits; ++sp)
-                if (sp < p.splits) { acc.x += v[sp].x; acc.y += v[sp].y; acc.z += v[sp].z; acc.w += v[sp].w; }
-            const float a[4] = {acc.x, acc.y, acc.z, acc.w};
-            uint16_t *o = p.out + (int64_t)(t.mb * kBM + r) * p.ldo + gcol;
+        for (int sp = 1; sp < kMaxSplits; ++sp)
+            if (sp < p.splits) { acc.x += v[sp].x; acc.y += v[sp].y; acc.z += v[sp].z; acc.w += v[sp].w; }
+        const float a[4] = {acc.x, acc.y, acc.z, acc.w};
+        uint32_t h[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float b = (p.bias != nullptr && gcol + e < p.n_out) ? __uint_as_float((uint32_t)p.bias[gcol + e] << 16)
+                                                                     : 0.0f;
+            h[e] = bf16_bits_rn(__fmaf_rn(a[e], alpha, b));
+        }
+        uint16_t *o = p.out + (int64_t)(t.mb * kBM + r) * p.ldo + gcol;
+        if (gcol + 4 <= p.n_out) {      // 8-byte aligned: rows start on 16 bytes, gcol % 4 == 0
+            *reinterpret_cast<uint2 *>(o) = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+        } else {
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-                if (gcol + e < p.n_out) {
-                    const float b = p.bias ? __uint_as_float((uint32_t)p.bias[gcol + e] << 16) : 0.0f;
-                    o[e] = (uint16_t)bf16_bits_rn(__fmaf_rn(a[e], alpha, b));
-                }
+                if (gcol + e < p.n_out) o[e] = (uint16_t)h[e];
         }
     }
 }
@@ -351,6 +376,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after_sync();
             acc_phase ^= 1;
             const int64_t row = (int64_t)t.mb * kBM + q * 32 + lane;
+            const int row0 = t.mb * kBM + q * 32;
+            // columns of this warp's slice that hold output, 0 when all of
+            // its 32 rows are at or past m (small m: most warps)
+            const int cols_here = p.m > row0 ? n_cols : 0;
             uint32_t r0[32], r1[32];
 
             if (p.splits > 1) {
@@ -358,14 +387,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // CTA's shared memory (the operand ring: every stage of the
                 // CTA's one work item has been consumed)
                 const uint32_t dst = smem_u32(smem) + (uint32_t)((row - t.mb * kBM) * kPartLd + hcol) * 4;
-                if (n_cols > 0) tmem_ld_32cols(acc, r0);
+                if (cols_here > 0) tmem_ld_32cols(acc, r0);
 #pragma unroll
                 for (int ch = 0; ch < kEpiCols / 32; ++ch) {
                     uint32_t(&cur)[32] = (ch & 1) ? r1 : r0;
                     uint32_t(&nxt)[32] = (ch & 1) ? r0 : r1;
-                    if (ch * 32 < n_cols) {                     // uniform across the warp
+                    if (ch * 32 < cols_here) {                  // uniform across the warp
                         tmem_ld_wait_regs(cur);
-                        if (ch + 1 < kEpiCols / 32 && (ch + 1) * 32 < n_cols)
+                        if (ch + 1 < kEpiCols / 32 && (ch + 1) * 32 < cols_here)
                             tmem_ld_32cols(acc + (ch + 1) * 32, nxt);
                         if (row < p.m) {
 #pragma unroll
@@ -382,14 +411,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 
             uint32_t packed[kEpiCols / 2];
-            if (n_cols > 0) tmem_ld_32cols(acc, r0);
+            if (cols_here > 0) tmem_ld_32cols(acc, r0);
 #pragma unroll
             for (int ch = 0; ch < kEpiCols / 32; ++ch) {
                 uint32_t(&cur)[32] = (ch & 1) ? r1 : r0;
                 uint32_t(&nxt)[32] = (ch & 1) ? r0 : r1;
-                if (ch * 32 < n_cols) {                         // uniform across the warp
+                if (ch * 32 < cols_here) {                      // uniform across the warp
                     tmem_ld_wait_regs(cur);
-                    if (ch + 1 < kEpiCols / 32 && (ch + 1) * 32 < n_cols) tmem_ld_32cols(acc + (ch + 1) * 32, nxt);
+                    if (ch + 1 < kEpiCols / 32 && (ch + 1) * 32 < cols_here) tmem_ld_32cols(acc + (ch + 1) * 32, nxt);
 #pragma unroll
                     for (int j = 0; j < 32; j += 2) {
                         float b0 = 0.0f, b1 = 0.0f;
@@ -410,15 +439,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (use_bias) mbar_arrive(&bias_empty[it & 1]);
             }
 
+            // A few rows (small m): each of their lanes writes its row from
+            // registers, 16 bytes at a time (rows start on 16 bytes, col_base
+            // % 128 == 0); no round trips through the staging buffer.
+            const int rows_here = min(32, p.m - row0);
+            if (cols_here > 0 && rows_here <= kDirectStoreRows) {
+                if (lane < rows_here) {
+                    uint16_t *o = p.out + (int64_t)(row0 + lane) * p.ldo + col_base;
+#pragma unroll
+                    for (int g = 0; g < kEpiCols / 8; ++g) {
+                        if (8 * g + 8 <= cols_here) {
+                            *reinterpret_cast<uint4 *>(o + 8 * g) =
+                                make_uint4(packed[4 * g], packed[4 * g + 1], packed[4 * g + 2], packed[4 * g + 3]);
+                        } else if (8 * g < cols_here) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                if (8 * g + e < cols_here)
+                                    o[8 * g + e] = (uint16_t)(packed[4 * g + e / 2] >> (16 * (e & 1)));
+                        }
+                    }
+                }
+                continue;
+            }
+
             // Store through shared memory and the TMA: 16-column chunks of this
             // warp's 32 rows x 128 columns; the TMA clips rows >= m and
             // columns >= n_out.  (Thread-per-row global stores would touch 32
             // rows per instruction and congest the SM's memory pipeline that
             // the MMA thread's barrier and issue traffic also uses.)
-            const int row0 = t.mb * kBM + q * 32;
 #pragma unroll
             for (int c = 0; c < kEpiCols / 16; ++c) {
-                if (c * 16 < n_cols) {                          // uniform across the warp
+                if (c * 16 < cols_here) {                       // uniform across the warp
                     if (lane == 0) bulk_wait_group_read<0>();   // the previous chunk's store has read the buffer
                     __syncwarp();
                     st_shared_v4(out_stage + lane * 32, packed[c * 8], packed[c * 8 + 1], packed[c * 8 + 2],
