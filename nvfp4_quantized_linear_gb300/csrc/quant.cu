@@ -257,6 +257,19 @@ __global__ void __launch_bounds__(kXfThreads, 1)
     const int num_tiles = (p.mp / kXfRows) * n_ct;
     // x is read once; the amax pass leaves it in L2 for the quantizer that follows
     const uint64_t x_pol = kAmaxOnly ? l2_policy_evict_normal() : l2_policy_evict_first();
+    // T (in 16-byte pieces, 8 consecutive n of one row i; T is 16-byte
+    // aligned) and gs are loaded first, all loads in flight at once: issued
+    // after the x tiles' copies they would queue behind ~20 MB of them and
+    // hold back the first tile by about 2 us.
+    constexpr int kPieces = (128 * 128 / 8 + kXfThreads - 1) / kXfThreads;
+    const int pieces = bs * bs / 8;
+    uint4 tv[kPieces];
+#pragma unroll
+    for (int u = 0; u < kPieces; ++u) {
+        const int c = (int)threadIdx.x + u * kXfThreads;
+        if (c < pieces) tv[u] = __ldg(reinterpret_cast<const uint4 *>(p.t) + c);
+    }
+    const float gs = kAmaxOnly ? 1.0f : __ldg(p.gs);   // the amax pass has no scale yet
     int pre_issued = 0;                           // (thread 0, the producer) stages issued before the role split
     if (threadIdx.x == 0) {
         griddep_launch_dependents();              // as in quant_kernel
@@ -283,19 +296,9 @@ __global__ void __launch_bounds__(kXfThreads, 1)
     }
     // T^T into shared memory: element T[i][n] -> row n, K index i, written
     // where the 128-byte swizzle puts it (16-byte chunk index XOR row % 8).
-    // Each thread first loads its 16-byte pieces of T (8 consecutive n of one
-    // row i; T is 16-byte aligned), all loads in flight at once, then scatters.
     uint8_t *sT = smem + kXfOffT;
     {
-        constexpr int kPieces = (128 * 128 / 8 + kXfThreads - 1) / kXfThreads;
         const int lg = 31 - __clz(bs);                    // bs = 2^lg
-        const int pieces = bs * bs / 8;
-        uint4 tv[kPieces];
-#pragma unroll
-        for (int u = 0; u < kPieces; ++u) {
-            const int c = (int)threadIdx.x + u * kXfThreads;
-            if (c < pieces) tv[u] = __ldg(reinterpret_cast<const uint4 *>(p.t) + c);
-        }
 #pragma unroll
         for (int u = 0; u < kPieces; ++u) {
             const int c = (int)threadIdx.x + u * kXfThreads;
@@ -315,7 +318,6 @@ __global__ void __launch_bounds__(kXfThreads, 1)
         }
     }
     fence_proxy_async_shared();                   // the MMAs read T^T through the async proxy
-    const float gs = kAmaxOnly ? 1.0f : __ldg(p.gs);   // the amax pass has no scale yet
     if (!kAmaxOnly) fill_inv_table(inv_tab, gs);
     if (warp == 1) {
         tmem_alloc(tmem_slot, kXfTmemCols);
