@@ -2,11 +2,14 @@
 eager calls, and weights reloaded in place (nvfp4_prepare_weight into the same
 buffers) or new activations copied into the captured input buffer take effect
 on the next replay -- the stable-address weight reload of the B12X backends
-page (关键源码片段: in-place weight reload for captured graphs)."""
+page (关键源码片段: in-place weight reload for captured graphs).  The last
+replay is also checked against the oracle (transform, dynamic scale and all)."""
+import numpy as np
 import pytest
 import torch
 
-from _helpers import dev_scalar, nv, require_library, syn
+import oracle
+from _helpers import assert_gemm_close, bf16_to_f64, dev_scalar, nv, require_library, syn
 
 pytestmark = pytest.mark.gpu
 
@@ -93,3 +96,17 @@ def test_linear_graph_replay_and_in_place_reload(m, k, n, bs, dynamic):
     torch.cuda.synchronize()
     nv.nvfp4_device_error()
     assert torch.equal(out, eager3), "replay with new activations differs"
+
+    # the replayed result against the oracle: reloaded weight w2, new activations
+    xb = syn.bf16_bits(x)
+    t_bits = syn.bf16_bits(t) if bs else None
+    gs_ref = oracle.act_global_scale(xb, t_bits, bs, k) if dynamic else float(gs.item())
+    if dynamic:
+        assert np.float32(gs.item()) == np.float32(gs_ref), "replayed dynamic global scale differs from the oracle's"
+        assert np.float32(alpha.item()) == np.float32(oracle.alpha(gs_ref, g2)), "replayed alpha differs"
+    if bs:
+        xb = oracle.transform(xb, t_bits, bs, k)
+    a, sa = oracle.quantize(xb, gs_ref, k=k)
+    b, sb = oracle.quantize(syn.bf16_bits(w2), g2, k=k)
+    ref = oracle.gemm(a, sa, b, sb, float(alpha.item()))
+    assert_gemm_close(bf16_to_f64(out), ref, f"graph replay m={m} bs={bs} dynamic={dynamic}")
