@@ -504,19 +504,19 @@ def run_ours(args, rank, world, local_rank):
                    "l2": f"inputs larger than L2 ({sum(l['x'].numel() * 2 for l in layers) / 1e9:.2f} GB of "
                          "activations per step)", "bias": False, "transform": None},
         "roofline": {"bound": "tensor", "kernel": f"{top_kernel} ({layers[top]['p'].name} launch)",
-                     "achieved": round(top_tflops, 2), "peak": round(fp4_peak_sustained, 1), "unit": "TFLOP/s",
-                     "frac": round(top_tflops / fp4_peak_sustained, 4),
+                     "achieved": round(top_tflops, 2), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
+                     "frac": round(top_tflops / fp4_peak, 4),
                      "traffic": (round(traffic) if traffic else None),
                      "algorithmic_bytes": gemm_bytes(layers[top]["p"]),
                      "flops_per_launch": layers[top]["p"].flops,
                      "all_gemm_launches_achieved": round(gemm_tflops, 2),
-                     "peak_note": (f"dense FP4 = sustained bf16 {peaks.get('bf16_tflops_sustained')} x "
-                                   f"{FP4_OVER_BF16:g} from {peak_src}: the figure for a kernel timed inside a long "
-                                   "step.  The per-kernel pass runs the whole step --steps times right after the "
-                                   "timed step loop, when the part is at its power cap (the Qwen gate_up GEMM "
-                                   "back to back: about 1223 us a launch for the first 20 launches, 1394 us after "
-                                   f"80).  Burst-based peak {fp4_peak:.0f} (frac_of_burst), nominal 13500"),
-                     "frac_of_burst": round(top_tflops / fp4_peak, 4),
+                     "peak_note": (f"dense FP4 = burst bf16 {peaks.get('bf16_tflops')} x {FP4_OVER_BF16:g} from "
+                                   f"{peak_src}: the kernel is timed by CUDA events in a sub-second region at the "
+                                   "clocks in 'clocks'.  Sustained-based peak "
+                                   f"{fp4_peak_sustained:.0f} (frac_of_sustained: the figure for a seconds-long "
+                                   "loop; the Qwen gate_up GEMM back to back takes about 1223 us a launch for its "
+                                   "first 20 launches and 1394 us after 80, at the power cap), nominal 13500"),
+                     "frac_of_sustained": round(top_tflops / fp4_peak_sustained, 4),
                      "frac_of_nominal_13p5": round(top_tflops / 13500.0, 4)},
         "act_quant": {"bound": "hbm", "kernel": "quant_kernel", "achieved": round(quant_gbs, 1),
                       "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(quant_gbs / peaks["hbm_gbs"], 4),
