@@ -57,20 +57,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return done != 0;
 }
 
-// Non-blocking test of the phase of `bar` with the given parity.
-__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
-{
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-
 // Wait for the phase of `bar` with the given parity to complete, for at most
 // `limit_ns` nanoseconds of wall time.  On expiry it sets bit `code` in
 // *err_flag (device memory) and returns false: every pipeline wait in this
@@ -212,13 +198,6 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar)
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
                  : "memory");
-}
-
-// Copy a 32-row x 16-byte matrix from shared memory into TMEM columns
-// [taddr, taddr+4), replicated into all four 32-lane quarters.
-__device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t src_desc)
-{
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(src_desc) : "memory");
 }
 
 // D(tmem) (+)= A(smem) * B(smem)^T with FP4 E2M1 operands and one UE4M3 scale
@@ -381,11 +360,6 @@ __device__ __forceinline__ void griddep_launch_dependents()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-__device__ __forceinline__ void tmem_ld_wait()
-{
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
 // Shared-memory matrix descriptor of a K-major operand tile stored with the
 // 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr)
@@ -395,24 +369,6 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr)
            | ((uint64_t)(1024 >> 4) << 32)        // stride byte offset: 8 rows x 128 B
            | ((uint64_t)1 << 46)                  // descriptor version for tcgen05
            | ((uint64_t)2 << 61);                 // layout: 128-byte swizzle
-}
-
-// Same for a tile stored with the 64-byte swizzle: rows of 64 bytes, 8-row
-// groups 512 bytes apart.
-__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr)
-{
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4)     // start address >> 4
-           | ((uint64_t)1 << 16)                  // leading byte offset (unused when swizzled)
-           | ((uint64_t)(512 >> 4) << 32)         // stride byte offset: 8 rows x 64 B
-           | ((uint64_t)1 << 46)                  // descriptor version for tcgen05
-           | ((uint64_t)4 << 61);                 // layout: 64-byte swizzle
-}
-
-// Descriptor of a 32-row x 16-byte scale tile, unswizzled: 8-row core
-// matrices of 128 contiguous bytes, 128 bytes apart.
-__device__ __forceinline__ uint64_t smem_desc_sf(uint32_t saddr)
-{
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(128 >> 4) << 32) | ((uint64_t)1 << 46);
 }
 
 // Instruction descriptor of the block-scaled MMA: E2M1 x E2M1, UE4M3 scales,
@@ -493,41 +449,6 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
-// Arrive (release at cluster scope) on an mbarrier given by its shared::cluster address.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
-{
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity)
-{
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-
-// Bounded wait (as mbar_wait) with cluster-scope acquire, for barriers that
-// receive arrivals from the peer CTA.
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, unsigned int *err_flag,
-                                                  unsigned int code, uint64_t limit_ns)
-{
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait_cluster(bar, parity)) return true;
-        if ((i & 255u) == 0 && global_timer_ns() - t0 > limit_ns) {
-            atomicOr(err_flag, code);
-            return false;
-        }
-    }
-}
-
 // Split cluster barrier (any thread, not necessarily warp-converged): every
 // thread of the cluster arrives once per phase, and a thread's wait returns
 // once all have arrived; release / acquire at cluster scope.
@@ -580,13 +501,6 @@ __device__ __forceinline__ void tc_commit_pair(uint64_t *bar)
 {
     asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
-}
-
-// Pair copy of a 32-row x 16-byte scale tile: each CTA copies the tile at this
-// shared-memory offset of its own into its own TMEM columns [taddr, taddr+4).
-__device__ __forceinline__ void tc_cp_pair_32x128b_warpx4(uint32_t taddr, uint64_t src_desc)
-{
-    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(src_desc) : "memory");
 }
 
 // Pair block-scaled MMA: D (M=256 split 128/128 over the two CTAs' TMEM) (+)=
