@@ -314,10 +314,10 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t *a_fp4, const uint8_t *a_sf, int64
  * bias and the bf16 rounding (no extra launch, no partials in memory).  The
  * result is deterministic, but its fp32 rounding order differs from the
  * unsplit GEMM's (both are within the GEMM's accuracy).
- * For m <= 4 without a transform (decode batch sizes) the quantizer runs
- * inside the GEMM: its activation warp quantizes each K stage of x into the
- * MMA's shared-memory tile itself (the workspace's activation area is then
- * not written).  Codes, scales and output are those of nvfp4_quant_act
+ * For m <= 16 without a transform (decode batch sizes) the quantizer runs
+ * inside the GEMM: its epilogue warps, idle until the accumulator is done,
+ * quantize each K stage of x into the MMA's shared-memory tile themselves
+ * (the workspace's activation area is then not written).  Codes, scales and output are those of nvfp4_quant_act
  * followed by nvfp4_gemm, bit for bit. */
 nvfp4_status nvfp4_linear(const void *x_bf16, int64_t m, int64_t k, int64_t ldx,
                           const float *gs_dev, const void *transform_bf16, int bs,

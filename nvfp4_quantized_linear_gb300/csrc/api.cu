@@ -299,7 +299,7 @@ int split_k_plan(const nvfp4::GemmParams &g, int num_sms, int *stages_per_split)
 enum GemmKernel { kGemmAuto = 0, kGemmOneCta = 1, kGemmPair = 2, kGemmOneCtaSplit = 3 };
 
 // nvfp4_linear's fused path (the GEMM quantizes x itself) for m up to this.
-constexpr int64_t kFusedLinearMaxRows = 4;
+constexpr int64_t kFusedLinearMaxRows = 16;
 
 nvfp4_status run_gemm(const uint8_t *a, const uint8_t *a_sf, int64_t m, const uint8_t *w, const uint8_t *w_sf,
                       int64_t n_w, int64_t n_out, int64_t k, const float *alpha, const void *bias, void *out,
@@ -601,10 +601,8 @@ nvfp4_status nvfp4_linear(const void *x_bf16, int64_t m, int64_t k, int64_t ldx,
     if ((st = current_device(&num_sms)) != NVFP4_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const nvfp4::QuantParams qp = quant_params(x_bf16, m, k, ldx, gs_dev, transform_bf16, bs, a_fp4, a_sf);
-    // Decode sizes: the GEMM quantizes its own activation (one warp, each K
-    // stage as its slice lands).  That warp keeps up with the weight stream
-    // up to four rows; at eight the quantizer kernel plus the GEMM was faster
-    // on the largest layer (Qwen gate_up; measured per layer, m = 1, 2, 4, 8).
+    // Decode sizes: the GEMM quantizes its own activation (its eight epilogue
+    // warps, each K stage as its slice lands, one 16-element block per lane).
     if (m <= kFusedLinearMaxRows && transform_bf16 == nullptr)
         return run_gemm(a_fp4, a_sf, m, w_fp4, w_sf, n_w, n_out, k, alpha_dev, bias_bf16, out_bf16, ldo, num_sms,
                         s, true, false, kGemmAuto, 0, 0, false, &qp);

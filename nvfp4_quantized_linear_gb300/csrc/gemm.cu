@@ -73,9 +73,8 @@ constexpr uint32_t kOffBias = kOffSfb + kStages * kSfbBytes;   // two tiles of b
 constexpr uint32_t kOutChunkBytes = 32 * 16 * 2;              // output staging: 32 rows x 16 columns bf16
 constexpr uint32_t kOffOut = kOffBias + 2 * kBN * 2;          // per epilogue warp: one staging chunk
 constexpr uint32_t kOffBar = kOffOut + 8 * kOutChunkBytes;
-constexpr uint32_t kOffInvTab = kOffBar + 256;          // fused linear: gs / e4m3(code) for the 128 codes
-constexpr uint32_t kSmemBytes = kOffInvTab + 512 + 1024;   // + alignment slack
-constexpr int kFusedMaxRows = 8;                           // the fused linear's largest m
+constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;      // + alignment slack
+constexpr int kFusedMaxRows = 16;                          // the fused linear's largest m
 constexpr int kXSliceRows = 16;                             // rows of the fused linear's activation copies
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemSf = 256;
@@ -197,93 +196,81 @@ __device__ __forceinline__ void cluster_reduce(const GemmParams &p, const Tile &
     }
 }
 
-// The activation side of the fused small-m linear (the whole of warp 0): for
-// every stage of this CTA's work items, fetch the stage's 256 columns of the
-// m <= kFusedMaxRows activation rows (bf16, one 2-D TMA of 16 rows x 256
-// columns, zeros past m and k) into bytes [2 KB, 10 KB) of the stage's own A
-// tile -- the rows 16..127 of that tile, which the MMA reads but whose scales
-// are zero -- then quantize them exactly as quant_kernel does (one 16-element
-// block per lane and round) into the tile's first 16 rows (128-byte rows with
-// the TMA's 128-byte swizzle, the layout of the MMA's descriptor) and the
-// block scales into the stage's four scale tiles, zeroed first so that rows
-// >= m contribute nothing (their A bytes are finite FP4 codes whatever they
-// hold).  Then the async-proxy fence and the stage's second `full` arrival.
-// The slice's copy is requested by the weight producer together with the
-// stage's weights, as soon as the stage frees (up to kStages ahead): a warp
-// that fetched each slice itself after quantizing the previous one paid the
-// copy's round trip once per stage.
+// The activation side of the fused small-m linear, run by the eight epilogue
+// warps (idle during the mainloop) before each work item's epilogue: for every
+// stage of the work item, the weight producer has fetched the stage's 256
+// columns of the m <= kFusedMaxRows activation rows (bf16, one 2-D TMA of 16
+// rows x 256 columns, zeros past m and k) into bytes [2 KB, 10 KB) of the
+// stage's own A tile -- rows 16..127 of that tile, which the MMA reads but
+// whose output rows are never stored.  Epilogue warp w quantizes block
+// 32 w + lane of the m x 16 blocks exactly as quant_kernel does into the
+// tile's first 16 rows (128-byte rows with the TMA's 128-byte swizzle, the
+// layout of the MMA's descriptor) and its scale into the stage's four scale
+// tiles, whose rows >= m were zeroed once at kernel start (their A bytes are
+// finite FP4 codes whatever they hold).  Then the async-proxy fence and the
+// warp's arrival on the stage's `full` barrier (eight of its nine).  One warp
+// quantizing every block fell behind the weight stream from m = 8 on.  The
+// slice's copy is requested by the weight producer together with the stage's
+// weights, as soon as the stage frees (up to kStages ahead): a warp that
+// fetched each slice itself after quantizing the previous one paid the copy's
+// round trip once per stage.  inv = gs / e4m3(code) with the IEEE division,
+// the value quant_kernel's table holds.  Returns false when a wait expired.
 constexpr uint32_t kXSliceOff = 16 * 128;                    // rows 16.. of an A tile
 constexpr uint32_t kXSliceBytes = kXSliceRows * 256 * 2;     // 16 rows x 256 bf16
 static_assert(kXSliceOff + kXSliceBytes <= kABytes, "the activation slice fits in the A tile's spare rows");
+static_assert(kFusedMaxRows * 16 <= kEpiWarps * 32, "one 16-element block per epilogue lane and stage");
 
-template <bool kFused>
-__device__ __forceinline__ void fused_act_producer(const GemmParams &p, uint8_t *smem, uint64_t *full,
-                                                   uint64_t *x_full, int num_ks, int lane)
+__device__ __forceinline__ bool fused_quant_stages(const GemmParams &p, uint8_t *smem, uint64_t *full,
+                                                   uint64_t *x_full, const Work &wk, int &stage, uint32_t &phase,
+                                                   float gs, int wq, int lane)
 {
-    griddep_wait();                                  // x and gs may be the preceding kernel's output
     const QuantParams &q = p.quant;
-    const float gs = __ldg(q.gs);
-    // gs / e4m3(code) for the 128 scale codes, built by this warp from the gs
-    // read after the wait (the preceding kernel may have written gs)
-    float *inv_tab = reinterpret_cast<float *>(smem + kOffInvTab);
-    for (int c = lane; c < 128; c += 32) {
-        const float d = e4m3_to_f32((uint32_t)c);
-        inv_tab[c] = (d == 0.0f) ? 0.0f : __fdiv_rn(gs, d);
-    }
-    __syncwarp();
-    int stage = 0;
-    uint32_t phase = 0;
-    for (int tile = blockIdx.x; tile < p.num_m_blk * p.num_n_blk * p.splits; tile += gridDim.x) {
-        const Work wk = work_of(tile, p, num_ks);
-        for (int ks = wk.ks0; ks < wk.ks1; ++ks) {
-            // the slice landed (it was requested after the stage freed, so the
-            // stage's A and scale tiles may be rewritten too)
-            if (!__all_sync(~0u, mbar_wait(&x_full[stage], phase, p.err_flag, kErrTimeout, p.wait_ns))) return;
-            uint8_t *a_tile = smem + kOffA + stage * kABytes;
-            const uint32_t a_dst = smem_u32(a_tile);
-            const uint32_t x_src = a_dst + kXSliceOff;
-            const uint32_t sf_dst = smem_u32(smem + kOffSfa + stage * kSfaBytes);
+    for (int ks = wk.ks0; ks < wk.ks1; ++ks) {
+        if (!__all_sync(~0u, mbar_wait(&x_full[stage], phase, p.err_flag, kErrTimeout, p.wait_ns))) return false;
+        const uint32_t a_dst = smem_u32(smem + kOffA + stage * kABytes);
+        const uint32_t x_src = a_dst + kXSliceOff;
+        const uint32_t sf_dst = smem_u32(smem + kOffSfa + stage * kSfaBytes);
+        const int b = wq * 32 + lane;
+        if (b < q.m * 16) {
+            const int r = b >> 4, j = b & 15;
+            quant_core::Raw16 raw;
+            raw.a = ld_shared_v4(x_src + (uint32_t)r * 512 + (uint32_t)j * 32);
+            raw.b = ld_shared_v4(x_src + (uint32_t)r * 512 + (uint32_t)j * 32 + 16);
+            float v0[8], v1[8];
+            quant_core::unpack8(raw.a, v0);
+            quant_core::unpack8(raw.b, v1);
+            float amax = 0.0f;
 #pragma unroll
-            for (int i = 0; i < (int)kSfaBytes / 16 / 32; ++i) st_shared_v4(sf_dst + (lane + 32 * i) * 16, 0, 0, 0, 0);
-            for (int b = lane; b < q.m * 16; b += 32) {
-                const int r = b >> 4, j = b & 15;
-                quant_core::Raw16 raw;
-                raw.a = ld_shared_v4(x_src + (uint32_t)r * 512 + (uint32_t)j * 32);
-                raw.b = ld_shared_v4(x_src + (uint32_t)r * 512 + (uint32_t)j * 32 + 16);
-                float v0[8], v1[8];
-                quant_core::unpack8(raw.a, v0);
-                quant_core::unpack8(raw.b, v1);
-                float amax = 0.0f;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(v0[i]), fabsf(v1[i])));
-                float inv;
-                const uint32_t sf = quant_core::block_scale_tab(amax, gs, inv_tab, inv);
-                const uint32_t lo = quant_core::quant8(v0, inv), hi = quant_core::quant8(v1, inv);
-                // packed bytes [8j, 8j + 8) of row r: 16-byte piece j / 2 of the
-                // row, at piece (j / 2) ^ (r % 8) after the swizzle
-                const uint32_t a_off = (uint32_t)(r >> 3) * 1024 + (uint32_t)(r & 7) * 128 +
-                                       ((uint32_t)((j >> 1) ^ (r & 7)) << 4) + (uint32_t)(j & 1) * 8;
-                asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(a_dst + a_off), "r"(lo), "r"(hi) : "memory");
-                // scale column j of the stage: tile j / 4, the tiled layout inside it
-                const uint32_t sf_off = (uint32_t)(j >> 2) * 512 + (uint32_t)(r & 31) * 16 + (uint32_t)((r >> 5) & 3) * 4 +
-                                        (uint32_t)(j & 3);
-                asm volatile("st.shared.u8 [%0], %1;" ::"r"(sf_dst + sf_off), "r"(sf) : "memory");
-            }
-            fence_proxy_async_shared();                      // the MMA reads the A tile through the async proxy
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&full[stage]);
-            if (++stage == kStages) { stage = 0; phase ^= 1; }
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(v0[i]), fabsf(v1[i])));
+            const uint32_t sf = cvt_e4m3x2(0.0f, div6_rn(__fmul_rn(amax, gs))) & 0x7Fu;
+            const float d = e4m3_to_f32(sf);
+            const float inv = (d == 0.0f) ? 0.0f : __fdiv_rn(gs, d);
+            const uint32_t lo = quant_core::quant8(v0, inv), hi = quant_core::quant8(v1, inv);
+            // packed bytes [8j, 8j + 8) of row r: 16-byte piece j / 2 of the
+            // row, at piece (j / 2) ^ (r % 8) after the swizzle
+            const uint32_t a_off = (uint32_t)(r >> 3) * 1024 + (uint32_t)(r & 7) * 128 +
+                                   ((uint32_t)((j >> 1) ^ (r & 7)) << 4) + (uint32_t)(j & 1) * 8;
+            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(a_dst + a_off), "r"(lo), "r"(hi) : "memory");
+            // scale column j of the stage: tile j / 4, the tiled layout inside it
+            const uint32_t sf_off = (uint32_t)(j >> 2) * 512 + (uint32_t)(r & 31) * 16 + (uint32_t)((r >> 5) & 3) * 4 +
+                                    (uint32_t)(j & 3);
+            asm volatile("st.shared.u8 [%0], %1;" ::"r"(sf_dst + sf_off), "r"(sf) : "memory");
         }
+        fence_proxy_async_shared();                          // the MMA reads the A tile through the async proxy
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[stage]);
+        if (++stage == kStages) { stage = 0; phase ^= 1; }
     }
+    return true;
 }
 
 // kMx: MXFP4 operands (one UE8M0 scale per 32 K-elements, two 512-byte scale
 // tiles per band and stage, scale_vec::2X MMAs); otherwise NVFP4 (one UE4M3
 // scale per 16 K-elements, four tiles per band and stage, scale_vec::4X).
 // kFused: the fused small-m linear (NVFP4, m <= kFusedMaxRows): no A tensor
-// is read; warp 0 quantizes each stage's slice of the activation p.quant.x
-// (the body of quant_kernel for the stage's 16 blocks of every row) straight
-// into the stage's A tile and scale tiles in shared memory.
+// is read; the epilogue warps quantize each stage's slice of the activation
+// p.quant.x (the body of quant_kernel for the stage's 16 blocks of every row)
+// straight into the stage's A tile and scale tiles in shared memory.
 template <bool kMx, bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -308,7 +295,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 2);             // the activation and the weight producer
+            // the activation and the weight producer (fused: the weight
+            // producer and the eight quantizing epilogue warps)
+            mbar_init(&full[s], kFused ? 1 + kEpiWarps : 2);
             mbar_init(&empty[s], 1);
             mbar_init(&sf_ready[s], 4);
         }
@@ -329,6 +318,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
+    }
+    if constexpr (kFused) {             // scale rows >= m stay zero in every stage
+        for (uint32_t o = threadIdx.x * 16; o < kStages * kSfaBytes; o += kThreads * 16)
+            st_shared_v4(smem_u32(smem + kOffSfa) + o, 0, 0, 0, 0);
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -361,9 +354,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t out_policy = l2_policy_evict_first();   // the output is written once
         uint32_t acc_phase = 0;
         int it = 0;
+        int q_stage = 0;                                        // fused linear: the quantized stages
+        uint32_t q_phase = 0;
+        float q_gs = 0.0f;
+        if constexpr (kFused) {
+            griddep_wait();                                     // x and gs may be the preceding kernel's output
+            q_gs = __ldg(p.quant.gs);
+        }
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
             const Work wk = work_of(tile, p, num_ks);
             if (wk.g < 0) continue;                             // every role skips the same tiles
+            // (a timeout drill quantizes nothing: its stages never fill)
+            if (kFused && !p.drill &&
+                !fused_quant_stages(p, smem, full, x_full, wk, q_stage, q_phase, q_gs, warp - kEpiWarp0, lane))
+                break;
             const float alpha = p.alpha != nullptr ? __ldg(p.alpha + wk.g) : 1.0f;
             const Tile t = wk.t;
             const int n_cols = min(kEpiCols, p.n_out - t.nb * kBN - hcol);   // may be <= 0
@@ -555,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         setmaxnreg_dec<kRegsCtl>();
         if (kFused && warp == 0) {
-            if (!p.drill) fused_act_producer<kFused>(p, smem, full, x_full, num_ks, lane);
+            // the fused linear reads no A tensor: the epilogue warps quantize it
         } else if ((warp == 0 || warp == 3) && lane == 0 && !p.drill) {   // (a timeout drill issues no copies)
             // ----------------------------------------------------- producers --
             // Two threads fill the ring, each with its half of every stage:
@@ -847,7 +851,7 @@ cudaError_t launch_gemm(const GemmParams &p, const uint8_t *a, const uint8_t *w,
 cudaError_t launch_linear_fused(const GemmParams &p, const uint8_t *w, int num_sms, cudaStream_t s, const char **why)
 {
     if (p.mx || p.m > kFusedMaxRows || p.quant.bs != 0 || p.group_offsets != nullptr) {
-        *why = "the fused linear takes NVFP4 activations of at most 8 rows, without a transform";
+        *why = "the fused linear takes NVFP4 activations of at most 16 rows, without a transform";
         return cudaErrorInvalidValue;
     }
     // A programmatic dependent of the kernel before it: the prologue (barrier

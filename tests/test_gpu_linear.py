@@ -167,13 +167,13 @@ def test_split_k_matches_oracle_and_unsplit(p):
     assert np.all(np.abs(split - unsplit) <= bound), "split-K and unsplit GEMM differ beyond rounding"
 
 
-@pytest.mark.parametrize("m", [1, 2, 3, 4, 5, 8, 9, 16, 77, 128])
+@pytest.mark.parametrize("m", [1, 2, 3, 4, 5, 8, 9, 13, 16, 17, 77, 128])
 def test_small_m_linear_equals_quantizer_then_gemm(m):
-    """For m <= 4 nvfp4_linear runs the fused linear: the GEMM's activation
-    warp quantizes each stage of x into shared memory itself (no quantizer
+    """For m <= 16 nvfp4_linear runs the fused linear: the GEMM's epilogue
+    warps quantize each stage of x into shared memory themselves (no quantizer
     launch); above that, the quantizer writes the workspace and the GEMM reads
     it.  The output must equal nvfp4_quant_act followed by nvfp4_gemm_ex with
-    the same split-K plan (kernel 3) bit for bit either way (and for m > 4 so
+    the same split-K plan (kernel 3) bit for bit either way (and for m > 16 so
     must the workspace's quantized activation)."""
     k, n = 4104, 768
     x = syn.bf16_normal((m, k), 1.0, 1400 + m, device="cuda")
@@ -193,7 +193,7 @@ def test_small_m_linear_equals_quantizer_then_gemm(m):
     torch.cuda.synchronize()
     nv.nvfp4_device_error()
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
-    if m > 4:
+    if m > 16:
         assert torch.equal(ws[:pk], a_fp4.view(-1))
         sf0 = (pk + 255) // 256 * 256
         assert torch.equal(ws[sf0:sf0 + a_sf.numel()], a_sf)
