@@ -361,13 +361,20 @@ __global__ void __launch_bounds__(kXfThreads, 1)
             for (int u = 0; u < kXfUnits; ++u) {
                 const uint32_t *a = v + 16 * u;
                 float y0[8], y1[8];
-                float amax = 0.0f;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     y0[j] = round_bf16(__uint_as_float(a[j]));
                     y1[j] = round_bf16(__uint_as_float(a[8 + j]));
-                    amax = fmaxf(amax, fmaxf(fabsf(y0[j]), fabsf(y1[j])));
                 }
+                // The block maximum of the rounded values is the rounded
+                // maximum of the fp32 sums (rounding to nearest is monotone
+                // and symmetric): eight three-input maxima on the sums, then
+                // one rounding, off the path of the element roundings.
+                float m = quant_core::max_abs3(__uint_as_float(a[0]), __uint_as_float(a[1]), __uint_as_float(a[2]));
+#pragma unroll
+                for (int j = 3; j < 15; j += 2) m = quant_core::max_abs3(m, __uint_as_float(a[j]), __uint_as_float(a[j + 1]));
+                m = quant_core::max_abs3(m, __uint_as_float(a[15]), __uint_as_float(a[15]));
+                const float amax = round_bf16(m);
                 if constexpr (kAmaxOnly) {
                     tmax = fmaxf(tmax, amax);
                     continue;

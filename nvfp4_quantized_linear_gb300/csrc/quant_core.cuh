@@ -20,6 +20,15 @@ namespace quant_core {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
+// max(|a|, |b|, |c|): the three-input max.abs.f32 of sm_100 and later (one
+// instruction where two two-input maxima with abs operands were needed).
+__device__ __forceinline__ float max_abs3(float a, float b, float c)
+{
+    float d;
+    asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
