@@ -91,9 +91,9 @@ cudaError_t launch_quant_transform(const QuantParams &p, int num_sms, cudaStream
 // the GEMM's weight-side loads then start before that kernel has finished.
 cudaError_t launch_gemm(const GemmParams &p, const uint8_t *a, const uint8_t *w, int num_sms, cudaStream_t s,
                         const char **why, bool dependent = false);
-// The fused small-m linear (m <= 8, NVFP4, no transform): p.quant describes
-// the bf16 activation; the GEMM's activation warp quantizes each stage of it
-// into shared memory itself, so no quantizer runs before it.  Launched as a
+// The fused small-m linear (m <= 16, NVFP4, no transform): p.quant describes
+// the bf16 activation; the GEMM's epilogue warps quantize each stage of it
+// into shared memory themselves, so no quantizer runs before it.  Launched as a
 // programmatic dependent of the kernel before it, whose completion both of its
 // producers wait for.
 cudaError_t launch_linear_fused(const GemmParams &p, const uint8_t *w, int num_sms, cudaStream_t s,

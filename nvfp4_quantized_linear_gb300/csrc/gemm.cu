@@ -599,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   p.sfa + t.mb * p.sfa_band_bytes + (int64_t)ks * kT * 512, sf_bytes, &full[stage], pol);
                     } else {
                         if constexpr (kFused) {
-                            // the stage's activation slice for the fused linear's activation warp
+                            // the stage's activation slice for the fused linear's quantizing warps
                             // (every column tile's CTAs read the same slices: keep them in L2)
                             mbar_arrive_expect_tx(&x_full[stage], kXSliceBytes);
                             tma_load_2d(smem + kOffA + stage * kABytes + kXSliceOff, &tmX, &x_full[stage], ks * 256, 0,
