@@ -202,7 +202,9 @@ nvfp4_status nvfp4_mxfp4_gemm(const uint8_t *a_fp4, const uint8_t *a_sf, int64_t
  * stream.  workspace: caller-owned device scratch of at least
  * align256(nvfp4_packed_bytes(m,k)) + align256(nvfp4_mxfp4_scale_bytes(m,k))
  * bytes (= nvfp4_mxfp4_linear_workspace_bytes); with m <= 128 the GEMM may
- * split K as nvfp4_linear does. */
+ * split K as nvfp4_linear does, and for m <= 16 the quantizer runs inside the
+ * GEMM (its epilogue warps quantize each K stage of x; the workspace's
+ * activation area is then not written), as in nvfp4_linear. */
 size_t nvfp4_mxfp4_linear_workspace_bytes(int64_t m, int64_t k, int64_t n_w);
 nvfp4_status nvfp4_mxfp4_linear(const void *x_bf16, int64_t m, int64_t k, int64_t ldx,
                                 const uint8_t *w_fp4, const uint8_t *w_sf, int64_t n_w, int64_t n_out,

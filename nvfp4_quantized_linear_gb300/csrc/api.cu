@@ -671,6 +671,10 @@ nvfp4_status nvfp4_mxfp4_linear(const void *x_bf16, int64_t m, int64_t k, int64_
     nvfp4::QuantParams p = quant_params(x_bf16, m, k, ldx, nullptr, nullptr, 0, a_fp4, a_sf);
     p.nb = (int32_t)(nvfp4::padded_k(k) / 32);
     p.nbp = (p.nb + 3) / 4 * 4;
+    // decode sizes: the GEMM quantizes its own activation, as nvfp4_linear's fused path
+    if (m <= kFusedLinearMaxRows)
+        return run_gemm(a_fp4, a_sf, m, w_fp4, w_sf, n_w, n_out, k, nullptr, bias_bf16, out_bf16, ldo, num_sms, s,
+                        true, false, kGemmAuto, 0, 0, true, &p);
     st = launch_status(nvfp4::launch_quant_mx(p, num_sms, s), "MXFP4 quantize kernel");
     if (st != NVFP4_OK) return st;
     return run_gemm(a_fp4, a_sf, m, w_fp4, w_sf, n_w, n_out, k, nullptr, bias_bf16, out_bf16, ldo, num_sms, s,

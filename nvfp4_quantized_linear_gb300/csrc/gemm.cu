@@ -214,12 +214,17 @@ __device__ __forceinline__ void cluster_reduce(const GemmParams &p, const Tile &
 // weights, as soon as the stage frees (up to kStages ahead): a warp that
 // fetched each slice itself after quantizing the previous one paid the copy's
 // round trip once per stage.  inv = gs / e4m3(code) with the IEEE division,
-// the value quant_kernel's table holds.  Returns false when a wait expired.
+// the value quant_kernel's table holds.  kMx (MXFP4, quant_mx_kernel's
+// arithmetic): a lane holds half of a 32-element block, the two halves' maxima
+// meet through one shuffle, and the even lane stores the block's UE8M0 code
+// (scale column j / 2 of the stage, two scale tiles).  Returns false when a
+// wait expired.
 constexpr uint32_t kXSliceOff = 16 * 128;                    // rows 16.. of an A tile
 constexpr uint32_t kXSliceBytes = kXSliceRows * 256 * 2;     // 16 rows x 256 bf16
 static_assert(kXSliceOff + kXSliceBytes <= kABytes, "the activation slice fits in the A tile's spare rows");
 static_assert(kFusedMaxRows * 16 <= kEpiWarps * 32, "one 16-element block per epilogue lane and stage");
 
+template <bool kMx>
 __device__ __forceinline__ bool fused_quant_stages(const GemmParams &p, uint8_t *smem, uint64_t *full,
                                                    uint64_t *x_full, const Work &wk, int &stage, uint32_t &phase,
                                                    float gs, int wq, int lane)
@@ -231,7 +236,9 @@ __device__ __forceinline__ bool fused_quant_stages(const GemmParams &p, uint8_t 
         const uint32_t x_src = a_dst + kXSliceOff;
         const uint32_t sf_dst = smem_u32(smem + kOffSfa + stage * kSfaBytes);
         const int b = wq * 32 + lane;
-        if (b < q.m * 16) {
+        // warps with any block of the m rows; their lanes past it (zero rows
+        // of the slice) compute too, for the shuffle, but store nothing
+        if (wq * 32 < q.m * 16) {
             const int r = b >> 4, j = b & 15;
             quant_core::Raw16 raw;
             raw.a = ld_shared_v4(x_src + (uint32_t)r * 512 + (uint32_t)j * 32);
@@ -242,19 +249,33 @@ __device__ __forceinline__ bool fused_quant_stages(const GemmParams &p, uint8_t 
             float amax = 0.0f;
 #pragma unroll
             for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(v0[i]), fabsf(v1[i])));
-            const uint32_t sf = cvt_e4m3x2(0.0f, div6_rn(__fmul_rn(amax, gs))) & 0x7Fu;
-            const float d = e4m3_to_f32(sf);
-            const float inv = (d == 0.0f) ? 0.0f : __fdiv_rn(gs, d);
+            uint32_t sf, sf_off;
+            float inv;
+            if constexpr (kMx) {
+                amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 1));   // the block's other half
+                sf = quant_core::mx_scale_code(amax);
+                inv = quant_core::mx_scale_mul(sf);
+                const int jb = j >> 1;                               // scale column of the stage
+                sf_off = (uint32_t)(jb >> 2) * 512 + (uint32_t)(r & 31) * 16 + (uint32_t)((r >> 5) & 3) * 4 +
+                         (uint32_t)(jb & 3);
+            } else {
+                sf = cvt_e4m3x2(0.0f, div6_rn(__fmul_rn(amax, gs))) & 0x7Fu;
+                const float d = e4m3_to_f32(sf);
+                inv = (d == 0.0f) ? 0.0f : __fdiv_rn(gs, d);
+                // scale column j of the stage: tile j / 4, the tiled layout inside it
+                sf_off = (uint32_t)(j >> 2) * 512 + (uint32_t)(r & 31) * 16 + (uint32_t)((r >> 5) & 3) * 4 +
+                         (uint32_t)(j & 3);
+            }
             const uint32_t lo = quant_core::quant8(v0, inv), hi = quant_core::quant8(v1, inv);
             // packed bytes [8j, 8j + 8) of row r: 16-byte piece j / 2 of the
             // row, at piece (j / 2) ^ (r % 8) after the swizzle
             const uint32_t a_off = (uint32_t)(r >> 3) * 1024 + (uint32_t)(r & 7) * 128 +
                                    ((uint32_t)((j >> 1) ^ (r & 7)) << 4) + (uint32_t)(j & 1) * 8;
-            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(a_dst + a_off), "r"(lo), "r"(hi) : "memory");
-            // scale column j of the stage: tile j / 4, the tiled layout inside it
-            const uint32_t sf_off = (uint32_t)(j >> 2) * 512 + (uint32_t)(r & 31) * 16 + (uint32_t)((r >> 5) & 3) * 4 +
-                                    (uint32_t)(j & 3);
-            asm volatile("st.shared.u8 [%0], %1;" ::"r"(sf_dst + sf_off), "r"(sf) : "memory");
+            if (b < q.m * 16) {
+                asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(a_dst + a_off), "r"(lo), "r"(hi) : "memory");
+                if (!kMx || (lane & 1) == 0)
+                    asm volatile("st.shared.u8 [%0], %1;" ::"r"(sf_dst + sf_off), "r"(sf) : "memory");
+            }
         }
         fence_proxy_async_shared();                          // the MMA reads the A tile through the async proxy
         __syncwarp();
@@ -267,10 +288,11 @@ __device__ __forceinline__ bool fused_quant_stages(const GemmParams &p, uint8_t 
 // kMx: MXFP4 operands (one UE8M0 scale per 32 K-elements, two 512-byte scale
 // tiles per band and stage, scale_vec::2X MMAs); otherwise NVFP4 (one UE4M3
 // scale per 16 K-elements, four tiles per band and stage, scale_vec::4X).
-// kFused: the fused small-m linear (NVFP4, m <= kFusedMaxRows): no A tensor
-// is read; the epilogue warps quantize each stage's slice of the activation
-// p.quant.x (the body of quant_kernel for the stage's 16 blocks of every row)
-// straight into the stage's A tile and scale tiles in shared memory.
+// kFused: the fused small-m linear (m <= kFusedMaxRows, NVFP4 or with kMx
+// MXFP4): no A tensor is read; the epilogue warps quantize each stage's slice
+// of the activation p.quant.x (the body of quant_kernel, or quant_mx_kernel,
+// for the stage's 256 columns of every row) straight into the stage's A tile
+// and scale tiles in shared memory.
 template <bool kMx, bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -359,14 +381,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         float q_gs = 0.0f;
         if constexpr (kFused) {
             griddep_wait();                                     // x and gs may be the preceding kernel's output
-            q_gs = __ldg(p.quant.gs);
+            if constexpr (!kMx) q_gs = __ldg(p.quant.gs);       // (MXFP4 has no global scale)
         }
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
             const Work wk = work_of(tile, p, num_ks);
             if (wk.g < 0) continue;                             // every role skips the same tiles
             // (a timeout drill quantizes nothing: its stages never fill)
             if (kFused && !p.drill &&
-                !fused_quant_stages(p, smem, full, x_full, wk, q_stage, q_phase, q_gs, warp - kEpiWarp0, lane))
+                !fused_quant_stages<kMx>(p, smem, full, x_full, wk, q_stage, q_phase, q_gs, warp - kEpiWarp0, lane))
                 break;
             const float alpha = p.alpha != nullptr ? __ldg(p.alpha + wk.g) : 1.0f;
             const Tile t = wk.t;
@@ -743,6 +765,9 @@ cudaError_t launch_one_cta(const GemmParams &p, const uint8_t *a, const uint8_t 
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(gemm_nvf4_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)kSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gemm_nvf4_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kSmemBytes);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
@@ -795,7 +820,9 @@ cudaError_t launch_one_cta(const GemmParams &p, const uint8_t *a, const uint8_t 
         *why = "cuTensorMapEncodeTiled failed for the activation";
         return cudaErrorInvalidValue;
     }
-    if (fused) return cudaLaunchKernelEx(&cfg, gemm_nvf4_kernel<false, true>, tmA, tmB, tmOut, tmX, p);
+    if (fused)
+        return p.mx ? cudaLaunchKernelEx(&cfg, gemm_nvf4_kernel<true, true>, tmA, tmB, tmOut, tmX, p)
+                    : cudaLaunchKernelEx(&cfg, gemm_nvf4_kernel<false, true>, tmA, tmB, tmOut, tmX, p);
     return p.mx ? cudaLaunchKernelEx(&cfg, gemm_nvf4_kernel<true, false>, tmA, tmB, tmOut, tmX, p)
                 : cudaLaunchKernelEx(&cfg, gemm_nvf4_kernel<false, false>, tmA, tmB, tmOut, tmX, p);
 }
@@ -850,8 +877,8 @@ cudaError_t launch_gemm(const GemmParams &p, const uint8_t *a, const uint8_t *w,
 
 cudaError_t launch_linear_fused(const GemmParams &p, const uint8_t *w, int num_sms, cudaStream_t s, const char **why)
 {
-    if (p.mx || p.m > kFusedMaxRows || p.quant.bs != 0 || p.group_offsets != nullptr) {
-        *why = "the fused linear takes NVFP4 activations of at most 16 rows, without a transform";
+    if (p.m > kFusedMaxRows || p.quant.bs != 0 || p.group_offsets != nullptr) {
+        *why = "the fused linear takes activations of at most 16 rows, without a transform";
         return cudaErrorInvalidValue;
     }
     // A programmatic dependent of the kernel before it: the prologue (barrier

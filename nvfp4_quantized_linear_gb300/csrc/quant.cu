@@ -75,16 +75,8 @@ __global__ void __launch_bounds__(256) quant_kernel(const QuantParams p)
 // bit of a subnormal); 2^-s is built from bits (s <= 125 for finite input).
 // Lanes 0, 8, 16, 24 store the codes of four consecutive blocks as one word
 // of a 512-byte scale tile (the tiled layout of the NVFP4 scales, one column
-// per 32 elements); p.nb / p.nbp count these columns.
-__device__ __forceinline__ uint32_t mx_scale_code(float amax)
-{
-    if (amax == 0.0f) return 0;
-    const uint32_t u = __float_as_uint(amax);
-    const int e = (int)(u >> 23);                       // amax >= 0: no sign bit
-    const int fl = e != 0 ? e - 127 : -149 + (31 - __clz((int)u));
-    const int s = min(max(fl - 2, -127), 127);
-    return (uint32_t)(s + 127);
-}
+// per 32 elements); p.nb / p.nbp count these columns.  The scale code is
+// quant_core::mx_scale_code.
 
 template <int U>
 __global__ void __launch_bounds__(256) quant_mx_kernel(const QuantParams p)
@@ -121,8 +113,8 @@ __global__ void __launch_bounds__(256) quant_mx_kernel(const QuantParams p)
 #pragma unroll
             for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(v0[i]), fabsf(v1[i])));
             amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
-            const uint32_t code = mx_scale_code(amax);
-            const float mul = __uint_as_float((254u - code) << 23);     // 2^-s, s = code - 127 <= 125
+            const uint32_t code = quant_core::mx_scale_code(amax);
+            const float mul = quant_core::mx_scale_mul(code);          // 2^-s
             if (r < p.m && k0 < p.kp) {
                 uint2 pk;
                 pk.x = quant8(v0, mul);

@@ -29,6 +29,24 @@ __device__ __forceinline__ float max_abs3(float a, float b, float c)
     return d;
 }
 
+// MXFP4 scale code of a 32-element block with absolute maximum `amax`:
+//     s = clamp(floor(log2 amax) - 2, -127, 127)  (-127 for a zero block),
+//     code = s + 127 (UE8M0), and the elements are quantized as e2m1(v * 2^-s).
+// floor(log2 amax) comes from the fp32 bits (exponent field, or the top set
+// bit of a subnormal).
+__device__ __forceinline__ uint32_t mx_scale_code(float amax)
+{
+    if (amax == 0.0f) return 0;
+    const uint32_t u = __float_as_uint(amax);
+    const int e = (int)(u >> 23);                       // amax >= 0: no sign bit
+    const int fl = e != 0 ? e - 127 : -149 + (31 - __clz((int)u));
+    const int s = min(max(fl - 2, -127), 127);
+    return (uint32_t)(s + 127);
+}
+
+// 2^-s for a scale code (s = code - 127 <= 125 for finite input), built from bits.
+__device__ __forceinline__ float mx_scale_mul(uint32_t code) { return __uint_as_float((254u - code) << 23); }
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 

@@ -99,11 +99,14 @@ def test_mxfp4_gemm_exact_power_of_two_case_is_bit_exact():
     assert torch.equal(out.cpu().view(torch.int16), exact.float().to(torch.bfloat16).view(torch.int16))
 
 
-@pytest.mark.parametrize("m,k,n", [(1, 14336, 4096), (64, 4096, 2048)])
+@pytest.mark.parametrize("m,k,n", [(1, 14336, 4096), (3, 4104, 1024), (8, 4096, 6144), (16, 14336, 4096),
+                                   (17, 4104, 2048), (64, 4096, 2048)])
 def test_mxfp4_linear_split_k_matches_unsplit(m, k, n):
     """Small m: the MXFP4 linear splits K across the CTAs of a cluster (fp32
-    partials summed in shared memory); against the oracle and the unsplit
-    MXFP4 GEMM on the same quantized operands."""
+    partials summed in shared memory), and for m <= 16 the GEMM's epilogue
+    warps quantize x themselves (m = 17 and 64 run the quantizer kernel);
+    against the oracle and the unsplit MXFP4 GEMM on the same quantized
+    operands."""
     x = syn.bf16_normal((m, k), 1.0, 6200 + m, device="cuda")
     w = syn.bf16_normal((n, k), 0.02, 6201, device="cuda")
     w_fp4, w_sf = _quant(w)
