@@ -566,6 +566,31 @@ def run_ours(args, rank, world, local_rank):
     return result
 
 
+def _cpu_list(text: str) -> set:
+    """The CPUs of a sysfs list such as "0-3,8,10-11"."""
+    cpus = set()
+    for part in text.strip().split(","):
+        if part:
+            lo, _, hi = part.partition("-")
+            cpus.update(range(int(lo), int(hi or lo) + 1))
+    return cpus
+
+
+def gpu_local_cpus(torch, dev) -> set:
+    """The CPUs on the GPU's own NUMA node (its PCI device's local_cpulist in
+    sysfs) that this process may run on; empty when that cannot be read.
+    Pinned host buffers are placed on the node of the thread that first
+    touches them, and copies to and from a remote node cross the CPUs'
+    interconnect too."""
+    try:
+        props = torch.cuda.get_device_properties(dev)
+        bus = f"{props.pci_domain_id:04x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+        with open(f"/sys/bus/pci/devices/{bus}/local_cpulist") as f:
+            return _cpu_list(f.read()) & os.sched_getaffinity(0)
+    except (AttributeError, OSError, ValueError, RuntimeError):
+        return set()
+
+
 def run_e2e(args, layers, flops_step, barrier, slowest, world, stream):
     """Through the public API with host buffers: every step copies every layer's
     activation in from pinned host memory, runs nvfp4_linear and copies its
@@ -578,6 +603,13 @@ def run_e2e(args, layers, flops_step, barrier, slowest, world, stream):
 
     import nvfp4_quantized_linear_gb300 as nv
     steps = max(3, min(args.steps, 10))
+    # the host side of the copies on the GPU's NUMA node, where the node can be read
+    allowed = os.sched_getaffinity(0)
+    local = gpu_local_cpus(torch, torch.cuda.current_device())
+    if local and local != allowed:
+        os.sched_setaffinity(0, local)
+    host_cpus = (f"{len(local)} of {len(allowed)} usable CPUs, the GPU's NUMA node" if local
+                 else f"{len(allowed)} usable CPUs (the GPU's NUMA node unknown)")
     hx = [l["x"].cpu().pin_memory() for l in layers]
     ho = [torch.empty(l["out"].shape, dtype=torch.bfloat16).pin_memory() for l in layers]
     h2d = sum(h.numel() * 2 for h in hx)
@@ -634,11 +666,13 @@ def run_e2e(args, layers, flops_step, barrier, slowest, world, stream):
     torch.cuda.synchronize()
     barrier()
     t = slowest(e0.elapsed_time(e1) / 1e3 / steps)
+    os.sched_setaffinity(0, allowed)
     return {"value": round(aggregate(flops_step, world, t) / 1e12, 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": round(t * 1e3, 3),
             "pipeline": "copies in, nvfp4_linear and copies out on three streams, two device buffers per "
-                        "activation and output"}
+                        "activation and output",
+            "host_cpus": host_cpus}
 
 
 def run_sweep(args, rank, dev, stream):

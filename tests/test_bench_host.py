@@ -98,3 +98,10 @@ def test_reference_arm_json_line():
     assert d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == bench.host_cores()
     assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert d["metric"] == bench.METRIC
+
+
+def test_cpu_list_parser():
+    """sysfs CPU lists (the GPU's local_cpulist) as sets of CPU numbers."""
+    assert bench._cpu_list("0-3,8,10-11\n") == {0, 1, 2, 3, 8, 10, 11}
+    assert bench._cpu_list("5") == {5}
+    assert bench._cpu_list("") == set()
