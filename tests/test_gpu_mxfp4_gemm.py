@@ -122,3 +122,26 @@ def test_mxfp4_linear_split_k_matches_unsplit(m, k, n):
     ref = _oracle(x, w, None, k, rows, cols)
     for o, what in ((lin, "split"), (unsplit, "unsplit")):
         assert_gemm_close(bf16_to_f64(o)[rows][:, cols], ref, f"mxfp4 linear {what}")
+
+
+@pytest.mark.parametrize("m,k", [(1, 256), (7, 96), (16, 256), (16, 224)])
+def test_mxfp4_fused_linear_equals_quantizer_then_gemm(m, k):
+    """For m <= 16 the MXFP4 linear quantizes x inside the GEMM (its epilogue
+    warps, one half of a 32-element block per lane).  With K of one stage the
+    split-K plan has nothing to split, so the output must equal
+    nvfp4_mxfp4_quant_act followed by nvfp4_mxfp4_gemm bit for bit, and the
+    workspace's activation area stays untouched."""
+    n = 1024
+    x = syn.bf16_normal((m, k), 1.0, 6300 + m + k, device="cuda")
+    w = syn.bf16_normal((n, k), 0.02, 6301, device="cuda")
+    b = syn.bf16_normal((n,), 0.1, 6302, device="cuda")
+    w_fp4, w_sf = _quant(w)
+    ws = torch.full((nv.nvfp4_mxfp4_linear_workspace_bytes(m, k, n),), 0xA5, dtype=torch.uint8, device="cuda")
+    lin = nv.mxfp4_linear(x, w_fp4, w_sf, k, n, bias=b, workspace=ws)
+    a_fp4, a_sf = _quant(x)
+    ref = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+    nv.nvfp4_mxfp4_gemm(a_fp4, a_sf, m, w_fp4, w_sf, n, n, k, b, ref, n)
+    torch.cuda.synchronize()
+    nv.nvfp4_device_error()
+    assert torch.equal(lin.view(torch.int16), ref.view(torch.int16))
+    assert bool((ws == 0xA5).all()), "the fused path writes no quantized activation to the workspace"
